@@ -1,0 +1,306 @@
+"""fp64 CPU oracle of the LatentMoE layer: routing, permute, grouped SwiGLU
+experts, weighted combine, latent projections, and their backward.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path may import this module:
+only the tests, the smoke check of ``__graft_entry__`` and the CPU-baseline leg
+of ``bench.py`` use it. It shares no code with the CUDA library.
+
+All arithmetic is float64 with no intermediate rounding; inputs are the bf16
+(or fp32) values widened exactly. numpy's matmul and sort serve as library
+steps; there is no blocking, fusion or reordering beyond the definitions.
+
+Sources (the pages give the structure, not the formulas):
+  [MOE-A] "昇腾实现Kimi K3.1 Pro模型LoRA训练适配" page, section
+          "Kimi K3.1 Pro——面向长程智能体的开源旗舰大模型": 896 routed experts,
+          16 activated per token.
+  [MOE-B] "TorchTitan Ascend开源" page, section "Kimi K3.1 Pro 模型结构",
+          LatentMoE paragraph: 896 routed + 2 shared experts, 16 active, expert
+          compute in a low-dimensional latent space.
+  [MOE-C] "昇腾实现Kimi K3.1 Pro模型LoRA训练适配" page, section
+          "MoE(Mixture of Experts):算子融合与通信协同": dynamic routing, token
+          dispatch, Permute / Unpermute / Grouped GEMM as the core operators.
+  [MOE-D] "TorchTitan Ascend开源" page, section "在线负载规划": per-expert load
+          counted from the current routing result.
+Readings where the pages are silent (router = sigmoid(x@Wr) with renormalised
+top-k weights, lower expert id wins ties, tokens of an expert in ascending
+token order, shared experts in latent space with weight 1, routing weight
+applied to the expert output) are the plainest ones the workload statements
+support; each function below states the one it uses.
+
+Parity pins: every function here is pinned by tests/test_oracle_*.py against
+brute force, closed forms, invariants or finite differences; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "router_logits", "topk_select", "sigmoid", "routing_weights", "expert_counts",
+    "expert_offsets", "permutation_maps", "permute_rows", "swiglu_expert",
+    "grouped_swiglu", "combine", "layer_forward", "layer_backward",
+    "ep_rank_forward", "m_tiles_schedule",
+]
+
+
+def _f64(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        import torch  # only to widen torch inputs exactly
+        a = a.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Routing  [MOE-A], [MOE-C]
+# --------------------------------------------------------------------------
+
+def router_logits(x, Wr, bias=None) -> np.ndarray:
+    """L[t,e] = sum_i x[t,i] Wr[i,e] (+ b[e]).  The router reads the model-width
+    activations x (not the latent z); the optional per-expert bias is part of
+    the logit and so moves both the selection and the weights."""
+    L = _f64(x) @ _f64(Wr)
+    if bias is not None:
+        L = L + _f64(bias)[None, :]
+    return L
+
+
+def topk_select(L, k: int) -> np.ndarray:
+    """Ids of the k largest logits per token, ordered by (logit desc, id asc).
+
+    Selecting on the logit equals selecting on sigmoid(logit) (strictly
+    increasing) without the saturation ties of the sigmoid. A stable sort of
+    the negated logits keeps equal values in ascending id order, so the lower
+    id wins a tie. Returns int64 [T,k]."""
+    L = _f64(L)
+    order = np.argsort(-L, axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def sigmoid(v) -> np.ndarray:
+    v = _f64(v)
+    return 1.0 / (1.0 + np.exp(-v))
+
+
+def routing_weights(L, idx):
+    """s_j = sigmoid(L[t, idx_j]); w_j = s_j / sum_j' s_j' (no scale, no eps:
+    sigmoid > 0 so the sum is positive). Returns (w, s), both [T,k]."""
+    s = sigmoid(np.take_along_axis(_f64(L), np.asarray(idx), axis=1))
+    return s / s.sum(axis=1, keepdims=True), s
+
+
+# --------------------------------------------------------------------------
+# Permute bookkeeping  [MOE-C], [MOE-D]
+# --------------------------------------------------------------------------
+
+def expert_counts(idx, E: int) -> np.ndarray:
+    """counts[e] = number of (token, slot) pairs routed to expert e."""
+    counts = np.zeros(E, dtype=np.int64)
+    np.add.at(counts, np.asarray(idx).reshape(-1), 1)
+    return counts
+
+
+def expert_offsets(counts) -> np.ndarray:
+    """Exclusive prefix sum, E+1 entries; offsets[E] = T*k."""
+    c = np.asarray(counts, dtype=np.int64)
+    out = np.zeros(c.size + 1, dtype=np.int64)
+    out[1:] = np.cumsum(c)
+    return out
+
+
+def permutation_maps(idx, E: int):
+    """Stable counting sort of the (token, slot) pairs by expert.
+
+    Rows of expert e occupy [offsets[e], offsets[e+1]) of the permuted buffer,
+    tokens in ascending order (a token routes to an expert at most once, so
+    (e, t) is a unique key). Returns (slot_of [T,k], token_of [T*k], offsets)."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    offsets = expert_offsets(expert_counts(idx, E))
+    flat_e = idx.reshape(-1)                      # pair p = t*k + j, ascending t
+    order = np.argsort(flat_e, kind="stable")     # by expert, then by p
+    slot_of = np.empty(T * k, dtype=np.int64)
+    slot_of[order] = np.arange(T * k)
+    token_of = order // k
+    return slot_of.reshape(T, k), token_of.astype(np.int64), offsets
+
+
+def m_tiles_schedule(counts, tile_m: int = 128) -> np.ndarray:
+    """Exclusive prefix sum of ceil(counts[e] / tile_m), E+1 entries: the row-tile
+    index range of each expert in a grouped GEMM with tile_m-row tiles."""
+    c = np.asarray(counts, dtype=np.int64)
+    tiles = (c + tile_m - 1) // tile_m
+    out = np.zeros(c.size + 1, dtype=np.int64)
+    out[1:] = np.cumsum(tiles)
+    return out
+
+
+def permute_rows(z, token_of) -> np.ndarray:
+    """z_perm[r] = z[token_of[r]]."""
+    return _f64(z)[np.asarray(token_of)]
+
+
+# --------------------------------------------------------------------------
+# Experts  [MOE-B], [MOE-C]
+# --------------------------------------------------------------------------
+
+def _silu(g):
+    return g / (1.0 + np.exp(-g))
+
+
+def swiglu_expert(zrows, W13e, W2e, return_parts: bool = False):
+    """o = (silu(z W_gate) * (z W_up)) W2 with W13e = [W_gate | W_up] ([l, 2f])."""
+    zrows, W13e, W2e = _f64(zrows), _f64(W13e), _f64(W2e)
+    f = W2e.shape[0]
+    gu = zrows @ W13e
+    g, u = gu[:, :f], gu[:, f:]
+    h = _silu(g) * u
+    o = h @ W2e
+    if return_parts:
+        return o, g, u, h
+    return o
+
+
+def grouped_swiglu(z_perm, W13, W2, offsets, row_w=None):
+    """y_perm[r] = row_w[r] * swiglu_expert(z_perm[r], W13[e], W2[e]) for the
+    expert e whose segment [offsets[e], offsets[e+1]) holds r. Empty segments
+    contribute nothing. row_w=None means weight 1."""
+    z_perm = _f64(z_perm)
+    y = np.zeros((z_perm.shape[0], _f64(W2[0]).shape[1]))
+    E = len(offsets) - 1
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            y[a:b] = swiglu_expert(z_perm[a:b], W13[e], W2[e])
+    if row_w is not None:
+        y *= _f64(row_w)[:, None]
+    return y
+
+
+def combine(y_perm, slot_of, y_shared=None):
+    """y[t] = sum_j y_perm[slot_of[t,j]] (+ y_shared[t])."""
+    y_perm = _f64(y_perm)
+    y = y_perm[np.asarray(slot_of)].sum(axis=1)
+    if y_shared is not None:
+        y = y + _f64(y_shared)
+    return y
+
+
+# --------------------------------------------------------------------------
+# Whole layer
+# --------------------------------------------------------------------------
+
+def layer_forward(inp: dict, k: int | None = None, T: slice | None = None) -> dict:
+    """Forward of the latent MoE layer on the bf16 inputs of `inp`.
+
+    out = (y_sh + sum_j w_j o_j) W_up with z = x W_dn, o_j = expert_j(z),
+    y_sh = sum_s SwiGLU_s(z) (shared experts in latent space, weight 1),
+    routing on x as above. Returns every intermediate (fp64)."""
+    cfg = inp["cfg"]
+    k = cfg.k if k is None else k
+    x = _f64(inp["x"])
+    E = cfg.E
+    L = router_logits(x, inp["Wr"], inp.get("bias"))
+    idx = topk_select(L, k)
+    w, s = routing_weights(L, idx)
+    z = x @ _f64(inp["W_dn"])
+    slot_of, token_of, offsets = permutation_maps(idx, E)
+    z_perm = permute_rows(z, token_of)
+    row_w = w.reshape(-1)[np.argsort(slot_of.reshape(-1))]    # row_w[slot_of[t,j]] = w[t,j]
+    y_perm = grouped_swiglu(z_perm, inp["W13"], inp["W2"], offsets, row_w)
+    y_sh = np.zeros_like(z)
+    for sidx in range(inp["W13_sh"].shape[0]):
+        y_sh += swiglu_expert(z, inp["W13_sh"][sidx], inp["W2_sh"][sidx])
+    y_lat = combine(y_perm, slot_of, y_sh)
+    out = y_lat @ _f64(inp["W_up"])
+    return dict(L=L, idx=idx, w=w, s=s, z=z, slot_of=slot_of, token_of=token_of,
+                offsets=offsets, counts=np.diff(offsets), z_perm=z_perm, row_w=row_w,
+                y_perm=y_perm, y_sh=y_sh, y_lat=y_lat, out=out)
+
+
+def _swiglu_backward(zrows, W13e, W2e, d_o):
+    """Chain rule through o = (silu(g) * u) W2, [g|u] = z W13.
+    Returns dz, dW13e, dW2e."""
+    zrows, W13e, W2e = _f64(zrows), _f64(W13e), _f64(W2e)
+    f = W2e.shape[0]
+    gu = zrows @ W13e
+    g, u = gu[:, :f], gu[:, f:]
+    sg = 1.0 / (1.0 + np.exp(-g))
+    silu = g * sg
+    h = silu * u
+    dW2e = h.T @ d_o
+    dh = d_o @ W2e.T
+    dg = dh * u * sg * (1.0 + g * (1.0 - sg))     # d silu / dg = s (1 + g (1 - s))
+    du = dh * silu
+    dgu = np.concatenate([dg, du], axis=1)
+    return dgu @ W13e.T, zrows.T @ dgu, dW2e
+
+
+def layer_backward(inp: dict, fwd: dict, dout=None) -> dict:
+    """Gradients of loss = sum(out * dout) (dout defaults to inp["g"]) with
+    respect to x and every weight, routing held at its forward choice (the
+    selection is piecewise constant; the router bias is a constant).
+
+    Returns dx, dWr, dW_dn, dW13, dW2, dW13_sh, dW2_sh, dW_up and the routing
+    weight gradient d_w [T,k] (fp64)."""
+    cfg = inp["cfg"]
+    E = cfg.E
+    g = _f64(inp["g"] if dout is None else dout)
+    x = _f64(inp["x"])
+    W_up, W_dn, Wr = _f64(inp["W_up"]), _f64(inp["W_dn"]), _f64(inp["Wr"])
+    # out = y_lat W_up
+    dy_lat = g @ W_up.T
+    dW_up = fwd["y_lat"].T @ g
+    z, z_perm, offsets = fwd["z"], fwd["z_perm"], fwd["offsets"]
+    token_of, slot_of, row_w = fwd["token_of"], fwd["slot_of"], fwd["row_w"]
+    # y_lat[t] = y_sh[t] + sum_j y_perm[slot_of[t,j]];  y_perm[r] = w_r o_r
+    dy_perm = dy_lat[token_of]
+    R = z_perm.shape[0]
+    dz_perm = np.zeros_like(z_perm)
+    d_row_w = np.zeros(R)
+    dW13 = np.zeros((E,) + tuple(inp["W13"].shape[1:]))
+    dW2 = np.zeros((E,) + tuple(inp["W2"].shape[1:]))
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b == a:
+            continue                                   # empty expert: zero gradient
+        o = swiglu_expert(z_perm[a:b], inp["W13"][e], inp["W2"][e])
+        d_row_w[a:b] = np.einsum("rc,rc->r", dy_perm[a:b], o)
+        d_o = dy_perm[a:b] * row_w[a:b, None]
+        dz_perm[a:b], dW13[e], dW2[e] = _swiglu_backward(z_perm[a:b], inp["W13"][e],
+                                                         inp["W2"][e], d_o)
+    S = inp["W13_sh"].shape[0]
+    dz = np.zeros_like(z)
+    dW13_sh = np.zeros((S,) + tuple(inp["W13_sh"].shape[1:]))
+    dW2_sh = np.zeros((S,) + tuple(inp["W2_sh"].shape[1:]))
+    for sidx in range(S):
+        dzs, dW13_sh[sidx], dW2_sh[sidx] = _swiglu_backward(z, inp["W13_sh"][sidx],
+                                                             inp["W2_sh"][sidx], dy_lat)
+        dz += dzs
+    dz += dz_perm[slot_of].sum(axis=1)
+    # routing weights: w_j = s_j / S_sum, s_j = sigmoid(L_j)
+    d_w = d_row_w[slot_of]                              # [T,k]
+    w, s = fwd["w"], fwd["s"]
+    ssum = s.sum(axis=1, keepdims=True)
+    ds = (d_w - (w * d_w).sum(axis=1, keepdims=True)) / ssum
+    dL_sel = ds * s * (1.0 - s)
+    T = x.shape[0]
+    dL = np.zeros((T, E))
+    np.put_along_axis(dL, fwd["idx"], dL_sel, axis=1)
+    dWr = x.T @ dL
+    dW_dn = x.T @ dz
+    dx = dz @ W_dn.T + dL @ Wr.T
+    return dict(dy_lat=dy_lat, dy_perm=dy_perm, d_row_w=d_row_w, d_w=d_w, dL=dL,
+                dz_perm=dz_perm, dz=dz, dx=dx, dWr=dWr, dW_dn=dW_dn, dW13=dW13,
+                dW2=dW2, dW13_sh=dW13_sh, dW2_sh=dW2_sh, dW_up=dW_up)
+
+
+def ep_rank_forward(z_perm, counts, W13, W2, w, perm):
+    """Expert compute of one expert-parallel rank on pre-permuted rows, then the
+    weighted return to arrival order: out[perm[r]] = w[r] * o[r], where o[r] is
+    the SwiGLU output of the expert owning row r. No cross-row reduction (the
+    per-token sum happens on the token's home rank)."""
+    offsets = expert_offsets(counts)
+    y = grouped_swiglu(z_perm, W13, W2, offsets, w)
+    out = np.empty_like(y)
+    out[np.asarray(perm)] = y
+    return out
