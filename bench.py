@@ -1,0 +1,417 @@
+"""Benchmark of the LatentMoE layer forward + backward on GB300 (libmoe).
+
+Workload: T=16384 tokens, d=4096, latent l=1024, E=896 routed experts top-16,
+2 shared experts (SwiGLU f=512), loss = sum(out * g): one step is the full
+forward and backward (all expert, shared, projection and router gradients).
+Inputs and weights are seeded synthetic bf16 (inputs.py), resident in HBM.
+
+Prints one JSON line. `value` is whole-job tokens/s (device-timed with CUDA
+events over exactly --steps steps after --warmup steps); `e2e` repeats the
+measurement with the step's inputs copied from pinned host memory and the
+input gradient copied back inside the timed region. Under torchrun each rank
+runs an independent replica (the layer has no cross-GPU exchange here).
+
+--impl reference times the fp64 CPU oracle instead (bounded token sample per
+step, host cores), on the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s fwd+bwd (896 experts, top-16); grouped GEMM % of BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+EXPERT_GEMMS = ("expert_gemm1_swiglu", "expert_gemm2_rowscale", "expert_dgrad2_swiglu_bwd",
+                "expert_wgrad2", "expert_dgrad1", "expert_wgrad1")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--wgrad", default="f32", choices=["f32", "bf16"])
+    ap.add_argument("--cpu-sample-tokens", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+def kernel_work(cfg, T):
+    """Algorithmic (flops, bytes) per launch of each kernel label at token count T."""
+    d, l, E, k, S, f = cfg.d, cfg.l, cfg.E, cfg.k, cfg.S, cfg.f
+    R = T * k
+    w13 = E * l * 2 * f * 2
+    w2 = E * f * l * 2
+    b = 2  # bf16 bytes
+    return {
+        "router_logits_gemm": (2 * T * d * E, T * d * b + d * E * b + T * E * 4),
+        "topk_sigmoid": (0, T * E * 4 + T * k * 12),
+        "latent_proj_gemm": (2 * T * d * l, T * d * b + d * l * b + T * l * b),
+        "permute_gather": (0, T * l * b + R * l * b + R * 4),
+        "expert_gemm1_swiglu": (2 * R * l * 2 * f, R * l * b + w13 + R * f * b + R * 2 * f * b),
+        "expert_gemm2_rowscale": (2 * R * f * l, R * f * b + w2 + R * l * b + R * 4),
+        "shared_gemm1_swiglu": (2 * T * l * 2 * f * S, T * l * b + S * l * 2 * f * b + T * S * 3 * f * b),
+        "shared_gemm2": (2 * T * S * f * l, T * S * f * b + S * f * l * b + T * l * b),
+        "combine": (0, R * l * b + 2 * T * l * b + R * 4),
+        "latent_proj_dgrad": (2 * T * d * l, T * d * b + d * l * b + T * l * b),
+        "latent_proj_wgrad": (2 * T * d * l, T * d * b + T * l * b + d * l * 4),
+        "combine_bwd_gather": (0, T * l * b + R * l * b + R * 4),
+        "expert_dgrad2_swiglu_bwd": (2 * R * l * f, R * l * b + w2 + R * 6 * f * b + R * f * b + R * 8),
+        "expert_wgrad2": (2 * R * f * l, R * f * b + R * l * b + E * f * l * 4),
+        "expert_dgrad1": (2 * R * 2 * f * l, R * 2 * f * b + w13 + R * l * b),
+        "expert_wgrad1": (2 * R * l * 2 * f, R * l * b + R * 2 * f * b + E * l * 2 * f * 4),
+        "shared_dgrad2_swiglu_bwd": (2 * T * l * S * f, T * l * b + S * f * l * b + T * S * 5 * f * b),
+        "shared_wgrad2": (2 * T * S * f * l, T * S * f * b + T * l * b + S * f * l * 4),
+        "shared_dgrad1": (2 * T * S * 2 * f * l, T * S * 2 * f * b + S * l * 2 * f * b + T * l * b),
+        "shared_wgrad1": (2 * T * l * S * 2 * f, T * l * b + T * S * 2 * f * b + S * l * 2 * f * 4),
+        "permute_bwd_sum": (0, R * l * b + 2 * T * l * b + R * 4),
+        "routing_weight_grad_reduce": (0, R * 8 + R * 4),
+        "router_bwd_dlogits": (0, T * k * 16 + T * E * b),
+        "router_dgrad": (2 * T * E * d, T * E * b + d * E * b + 2 * T * d * b),
+        "router_wgrad": (2 * T * d * E, T * d * b + T * E * b + d * E * 4),
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as fh:
+                m = json.load(fh)
+            return m, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak_val(peaks, *names):
+    for n in names:
+        v = peaks.get(n)
+        if isinstance(v, (int, float)):
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "median", "gbs", "tflops"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return None
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_moe_layer_topk_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(label, workload):
+    """Per-launch DRAM bytes of `label` from the committed ncu summary, or None
+    when none was taken for this workload on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as fh:
+            tab = json.load(fh)
+    except Exception:
+        return None
+    ent = tab.get(workload, {}).get(label)
+    if not ent or ent.get("source_hash") != source_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_sample_time(inp_cpu, n_tokens):
+    """Time the fp64 oracle's forward + backward on the first n_tokens tokens."""
+    import oracle as O
+    sub = dict(inp_cpu)
+    sub["x"] = inp_cpu["x"][:n_tokens]
+    sub["g"] = inp_cpu["g"][:n_tokens]
+    t0 = time.perf_counter()
+    fwd = O.layer_forward(sub)
+    O.layer_backward(sub, fwd)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    from sparse_moe_layer_topk_gb300 import inputs as I
+    cfg = I.CONFIGS[args.config]
+    line = {"impl": "reference", "metric": METRIC, "unit": "tokens/s", "higher_is_better": True}
+    if rank != 0:
+        return
+    inp = I.make_layer_inputs(cfg, T=args.cpu_sample_tokens)
+    n = args.cpu_sample_tokens
+    for _ in range(args.warmup):
+        oracle_sample_time(inp, n)
+    times = [oracle_sample_time(inp, n) for _ in range(args.steps)]
+    total = sum(times)
+    value = n * args.steps / total
+    cores = os.cpu_count()
+    line.update({
+        "value": value, "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total / args.steps, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "l": cfg.l, "E": cfg.E,
+                   "k": cfg.k, "S": cfg.S, "f": cfg.f,
+                   "sample": f"first {n} tokens of the workload per step, full weights"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} tokens fwd+bwd per step, {args.steps} steps"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    })
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from sparse_moe_layer_topk_gb300 import _lib as M
+    from sparse_moe_layer_topk_gb300 import build as B
+    from sparse_moe_layer_topk_gb300 import inputs as I
+    from sparse_moe_layer_topk_gb300.layer import LatentMoELayer, weights_to_device
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        B.build_library()
+    if world > 1:
+        dist.barrier()
+    M.load()
+    cfg = I.CONFIGS[args.config]
+    T = cfg.T
+    inp = I.make_layer_inputs(cfg)
+    wdt = M.MOE_DTYPE_F32 if args.wgrad == "f32" else M.MOE_DTYPE_BF16
+    layer = LatentMoELayer(weights_to_device(inp), T, cfg.k, wdt)
+    x = inp["x"].cuda()
+    g = inp["g"].cuda()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        layer.step(x, g)
+    torch.cuda.synchronize()
+    if int(layer.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(layer.err.item())}")
+
+    # ---- device-timed region
+    dev_uuid = None
+    try:
+        dev_uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        dev_uuid = str(local)
+    clocks = ClockSampler(dev_uuid)
+    M.moe_timing_report()  # drop anything recorded so far
+    M.moe_timing_enable(True)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        layer.step(x, g)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    M.moe_timing_enable(False)
+    per_kernel = M.moe_timing_report()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T * args.steps / (ms / 1000.0)
+    launches = sum(c for c, _ in per_kernel.values())
+
+    # ---- end to end: pinned host inputs in, input gradient out, every step
+    e2e = None
+    if not args.no_e2e:
+        xh = inp["x"].pin_memory()
+        gh = inp["g"].pin_memory()
+        dxh = torch.empty_like(xh).pin_memory()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            x.copy_(xh, non_blocking=True)
+            g.copy_(gh, non_blocking=True)
+            dx = layer.step(x, g)
+            dxh.copy_(dx, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * T * args.steps / (ems / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(xh.numel() * 2 + gh.numel() * 2),
+               "d2h_bytes_per_step": int(dxh.numel() * 2)}
+
+    if int(layer.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(layer.err.item())}")
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    hbm = _peak_val(peaks, "hbm_gbs", "hbm_GBs", "hbm") or FALLBACK_PEAKS["hbm_gbs"]
+    tc = (_peak_val(peaks, "bf16_tflops_sustained") or _peak_val(peaks, "bf16_tflops")
+          or FALLBACK_PEAKS["bf16_tflops_sustained"])
+    work = kernel_work(cfg, T)
+    top = max(per_kernel.items(), key=lambda kv: kv[1][1]) if per_kernel else None
+    roof = None
+    breakdown = {}
+    for name, (cnt, tot) in sorted(per_kernel.items(), key=lambda kv: -kv[1][1]):
+        fl, by = work.get(name, (0, 0))
+        avg_s = tot / cnt / 1000.0
+        breakdown[name] = {"launches": cnt, "avg_us": round(avg_s * 1e6, 2),
+                           "share": round(tot / sum(v[1] for v in per_kernel.values()), 4),
+                           "tflops": round(fl / avg_s / 1e12, 1) if fl else None,
+                           "gbs": round(by / avg_s / 1e9, 1)}
+    if top:
+        name, (cnt, tot) = top
+        fl, by = work.get(name, (0, 0))
+        avg_s = tot / cnt / 1000.0
+        ridge = tc * 1e12 / (hbm * 1e9)
+        if fl and fl / max(by, 1) >= ridge * 0.25:
+            roof = {"kernel": name, "bound": "tensor", "achieved": fl / avg_s / 1e12,
+                    "peak": tc, "unit": "TFLOP/s", "frac": fl / avg_s / 1e12 / tc}
+        else:
+            roof = {"kernel": name, "bound": "hbm", "achieved": by / avg_s / 1e9, "peak": hbm,
+                    "unit": "GB/s", "frac": by / avg_s / 1e9 / hbm}
+        roof["traffic"] = dram_traffic(name, cfg.name)
+        roof["avg_launch_us"] = avg_s * 1e6
+        roof["peak_source"] = f"{peak_src} ({'sustained' if roof['bound'] == 'tensor' else 'copy'})"
+    g_fl = sum(work[n][0] * per_kernel[n][0] for n in EXPERT_GEMMS if n in per_kernel)
+    g_ms = sum(per_kernel[n][1] for n in EXPERT_GEMMS if n in per_kernel)
+    grouped_pct = 100.0 * (g_fl / (g_ms / 1000.0) / 1e12) / tc if g_ms else None
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n = args.cpu_sample_tokens
+        secs = oracle_sample_time(inp, n)
+        cpu = {"value": n / secs, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"fwd+bwd of the first {n} tokens of the workload, full weights, "
+                         f"{secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "T": T, "d": cfg.d, "l": cfg.l, "E": cfg.E,
+                       "k": cfg.k, "S": cfg.S, "f": cfg.f, "wgrad_dtype": args.wgrad,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (2.8 GB of expert weights and >1 GB of "
+                             "activations streamed per step); no explicit flush"},
+            "roofline": roof,
+            "grouped_gemm_pct_bf16_peak": grouped_pct,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "kernels": breakdown,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -39,7 +39,7 @@ __all__ = [
     "router_logits", "topk_select", "sigmoid", "routing_weights", "expert_counts",
     "expert_offsets", "permutation_maps", "permute_rows", "swiglu_expert",
     "grouped_swiglu", "combine", "layer_forward", "layer_backward",
-    "ep_rank_forward", "m_tiles_schedule",
+    "ep_rank_forward", "m_tiles_schedule", "router_backward", "swiglu_expert_backward",
 ]
 
 
@@ -217,7 +217,7 @@ def layer_forward(inp: dict, k: int | None = None, T: slice | None = None) -> di
                 y_perm=y_perm, y_sh=y_sh, y_lat=y_lat, out=out)
 
 
-def _swiglu_backward(zrows, W13e, W2e, d_o):
+def swiglu_expert_backward(zrows, W13e, W2e, d_o):
     """Chain rule through o = (silu(g) * u) W2, [g|u] = z W13.
     Returns dz, dW13e, dW2e."""
     zrows, W13e, W2e = _f64(zrows), _f64(W13e), _f64(W2e)
@@ -266,32 +266,39 @@ def layer_backward(inp: dict, fwd: dict, dout=None) -> dict:
         o = swiglu_expert(z_perm[a:b], inp["W13"][e], inp["W2"][e])
         d_row_w[a:b] = np.einsum("rc,rc->r", dy_perm[a:b], o)
         d_o = dy_perm[a:b] * row_w[a:b, None]
-        dz_perm[a:b], dW13[e], dW2[e] = _swiglu_backward(z_perm[a:b], inp["W13"][e],
+        dz_perm[a:b], dW13[e], dW2[e] = swiglu_expert_backward(z_perm[a:b], inp["W13"][e],
                                                          inp["W2"][e], d_o)
     S = inp["W13_sh"].shape[0]
     dz = np.zeros_like(z)
     dW13_sh = np.zeros((S,) + tuple(inp["W13_sh"].shape[1:]))
     dW2_sh = np.zeros((S,) + tuple(inp["W2_sh"].shape[1:]))
     for sidx in range(S):
-        dzs, dW13_sh[sidx], dW2_sh[sidx] = _swiglu_backward(z, inp["W13_sh"][sidx],
+        dzs, dW13_sh[sidx], dW2_sh[sidx] = swiglu_expert_backward(z, inp["W13_sh"][sidx],
                                                              inp["W2_sh"][sidx], dy_lat)
         dz += dzs
     dz += dz_perm[slot_of].sum(axis=1)
-    # routing weights: w_j = s_j / S_sum, s_j = sigmoid(L_j)
     d_w = d_row_w[slot_of]                              # [T,k]
-    w, s = fwd["w"], fwd["s"]
-    ssum = s.sum(axis=1, keepdims=True)
-    ds = (d_w - (w * d_w).sum(axis=1, keepdims=True)) / ssum
-    dL_sel = ds * s * (1.0 - s)
-    T = x.shape[0]
-    dL = np.zeros((T, E))
-    np.put_along_axis(dL, fwd["idx"], dL_sel, axis=1)
+    dL = router_backward(d_w, fwd["w"], fwd["s"], fwd["idx"], E)
     dWr = x.T @ dL
     dW_dn = x.T @ dz
     dx = dz @ W_dn.T + dL @ Wr.T
     return dict(dy_lat=dy_lat, dy_perm=dy_perm, d_row_w=d_row_w, d_w=d_w, dL=dL,
                 dz_perm=dz_perm, dz=dz, dx=dx, dWr=dWr, dW_dn=dW_dn, dW13=dW13,
                 dW2=dW2, dW13_sh=dW13_sh, dW2_sh=dW2_sh, dW_up=dW_up)
+
+
+def router_backward(d_w, w, s, idx, E: int) -> np.ndarray:
+    """Gradient of the router logits from the routing-weight gradient d_w [T,k].
+
+    w_j = s_j / sum_i s_i gives dL/ds_j = (d_w_j - sum_i w_i d_w_i) / sum_i s_i;
+    s_j = sigmoid(L_j) gives ds_j/dL_j = s_j (1 - s_j). Unselected experts get
+    zero (the top-k choice is piecewise constant). Returns dense dL [T,E]."""
+    d_w, w, s = _f64(d_w), _f64(w), _f64(s)
+    ssum = s.sum(axis=1, keepdims=True)
+    ds = (d_w - (w * d_w).sum(axis=1, keepdims=True)) / ssum
+    dL = np.zeros((d_w.shape[0], E))
+    np.put_along_axis(dL, np.asarray(idx), ds * s * (1.0 - s), axis=1)
+    return dL
 
 
 def ep_rank_forward(z_perm, counts, W13, W2, w, perm):

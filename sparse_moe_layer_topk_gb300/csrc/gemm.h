@@ -1,0 +1,85 @@
+// Host interface of the tcgen05 GEMM engine shared by every contraction of the
+// layer (router logits, latent projections, grouped SwiGLU experts and all of
+// their dgrad / wgrad products).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+enum GemmSched : int {
+  SCHED_DENSE = 0,      // one M x N x K problem
+  SCHED_GROUPED_M = 1,  // G problems over row segments offsets[g]..offsets[g+1] (ragged M)
+  SCHED_GROUPED_K = 2,  // G problems whose K runs over rows offsets[g]..offsets[g+1] (ragged K)
+};
+
+enum GemmEpi : int {
+  EPI_STORE = 0,       // C = acc (fp32 or bf16), or C += acc for bf16 with accumulate
+  EPI_SWIGLU = 1,      // h = silu(gate) * up (+ bf16 copy of gate|up)
+  EPI_ROWSCALE = 2,    // C = row_w[row] * acc (bf16)
+  EPI_SWIGLU_BWD = 3,  // dgrad of SwiGLU + routing-weight partial dots
+};
+
+// B operand batch selection (3-D tensor map, third coordinate).
+enum GemmBatch : int {
+  BATCH_NONE = 0,
+  BATCH_GROUP = 1,   // batch = group index g
+  BATCH_FROM_N = 2,  // batch = n_tile / n_tiles_per_batch
+  BATCH_FROM_K = 3,  // batch = k / k_per_batch
+};
+
+// A row-major bf16 matrix in device memory: [batch][rows][cols], cols contiguous.
+struct MatView {
+  const void* ptr = nullptr;
+  long long rows = 0, cols = 0;
+  long long ld = 0;            // elements between rows
+  long long batch = 1;         // >1 (or force3d) gives a 3-D tensor map
+  long long batch_stride = 0;  // elements between batches
+};
+
+struct GemmLaunch {
+  const char* name = "gemm";  // label of the launch in the optional per-kernel timing
+  int BN = 256;  // 128 or 256
+  int sched = SCHED_DENSE;
+  int M = 0, N = 0, K = 0, G = 1;
+  const int* offsets = nullptr;     // [G+1]
+  const int* tile_sched = nullptr;  // [G+1] (SCHED_GROUPED_M)
+  int R_cap = 0;                    // row capacity (SCHED_GROUPED_M grid bound)
+  // operands: A is [M][K] (a_mn = 0) or [K][M] (a_mn = 1);
+  //           B is [N][K] (b_mn = 0) or [K][N] (b_mn = 1), optionally batched.
+  MatView A, B;
+  int a_mn = 0, b_mn = 0;
+  int b_batch_mode = BATCH_NONE;
+  int n_tiles_per_batch = 0;
+  int k_per_batch = 0;
+  int swiglu_b = 0;  // B tile = BN/2 gate columns + BN/2 up columns (f apart)
+  int f = 0;
+  int n_tiles = 0;   // override of ceil(N / BN) (swiglu: h columns / (BN/2))
+  // epilogue
+  int epi = EPI_STORE;
+  void* C = nullptr;
+  long long ldc = 0;
+  long long c_batch_stride = 0;  // SCHED_GROUPED_K: per group; EPI_STORE + c_batch_n: per N block
+  int c_batch_n = 0;
+  int c_bf16 = 1;
+  int accumulate = 0;
+  const float* row_w = nullptr;
+  void* gu = nullptr;  // bf16
+  long long ldgu = 0;
+  void* h = nullptr;  // bf16
+  long long ldh = 0;
+  void* aux = nullptr;  // bf16
+  long long ldaux = 0;
+  float* dw_part = nullptr;
+  int dw_nparts = 0;
+  int* err_flag = nullptr;
+};
+
+// Returns MOE_OK or an MOE_ERR_* code (argument checks, launch errors).
+int gemm_launch(const GemmLaunch& L, cudaStream_t stream);
+
+int num_sms();
+void record_cuda_error(cudaError_t e);
+
+}  // namespace moe

@@ -1,0 +1,439 @@
+// Routing, permute bookkeeping and row-movement kernels of libmoe (sm_103a).
+//
+//   topk_sigmoid_kernel   warp per token: top-k of (logit + bias) by warp
+//                         redux over 64-bit (value, ~id) keys, then sigmoid
+//                         and renormalisation.
+//   chunk_hist_kernel     per 256-token chunk: one bit per (expert, token) in
+//                         shared memory -> per-chunk expert histogram.
+//   scan_kernel           one CTA: per-expert prefix over chunks, exclusive
+//                         scan over experts (offsets), 128-row tile schedule.
+//   maps_kernel           slot = chunk base + popcount of the expert's token
+//                         bits below this token: stable, atomics-free ranks.
+//   gather_rows_kernel    dst[r] = src[index[r]] with 16-byte vectors (permute,
+//                         combine backward).
+//   gather_sum_kernel     out[t] = sum_j src[slot[t][j]] (+ add[t]) in fp32
+//                         (combine, permute backward).
+//   router_bwd_kernel     routing-weight gradient -> dense bf16 dL row.
+//
+// Sources: token Permute / Unpermute of the "昇腾实现Kimi K3.1 Pro模型LoRA训练适配"
+// page, section "MoE(Mixture of Experts):算子融合与通信协同"; the per-expert load
+// count of the "TorchTitan Ascend开源" page, section "在线负载规划"; top-16 of 896
+// routed experts from section "Kimi K3.1 Pro 模型结构" of the same page.
+#include "common.cuh"
+#include "kernels.h"
+#include "timing.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kChunk = 256;  // tokens per chunk of the histogram / maps kernels
+
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(256) topk_sigmoid_kernel(const float* __restrict__ L,
+                                                           const float* __restrict__ bias, int T,
+                                                           int E, int k, int* __restrict__ idx,
+                                                           float* __restrict__ w_out,
+                                                           float* __restrict__ s_out,
+                                                           int* err_flag) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = L + static_cast<size_t>(t) * E;
+  uint32_t hi[NPL], lo[NPL];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float v = __ldg(row + e) + (bias ? __ldg(bias + e) : 0.0f);
+      bad |= !isfinite(v);
+      hi[i] = order_key(v);
+      lo[i] = ~static_cast<uint32_t>(e);  // larger for the lower id
+    } else {
+      hi[i] = 0u;
+      lo[i] = 0u;
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_flag(err_flag, MOE_FLAG_NONFINITE);
+  // local best (hi, lo) lexicographic
+  uint32_t bh = 0, bl = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (hi[i] > bh || (hi[i] == bh && lo[i] > bl)) { bh = hi[i]; bl = lo[i]; }
+  float my_v = 0.0f;
+  int my_e = -1;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t mh = __reduce_max_sync(0xFFFFFFFFu, bh);
+    const uint32_t ml = __reduce_max_sync(0xFFFFFFFFu, bh == mh ? bl : 0u);
+    if (bh == mh && bl == ml) {  // the unique winner lane removes its entry
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (hi[i] == mh && lo[i] == ml) { hi[i] = 0u; lo[i] = 0u; }
+      bh = 0;
+      bl = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (hi[i] > bh || (hi[i] == bh && lo[i] > bl)) { bh = hi[i]; bl = lo[i]; }
+    }
+    if (lane == j) {
+      my_v = key_value(mh);
+      my_e = static_cast<int>(~ml);
+    }
+  }
+  const float s = (lane < k) ? 1.0f / (1.0f + expf(-my_v)) : 0.0f;
+  float sum = s;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if (lane < k) {
+    const size_t o = static_cast<size_t>(t) * k + lane;
+    idx[o] = my_e;
+    s_out[o] = s;
+    w_out[o] = s / sum;
+  }
+}
+
+__device__ __forceinline__ void build_bits(uint32_t* bits, const int* __restrict__ idx, int T,
+                                           int E, int k, int* err_flag, bool check) {
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  const int t = blockIdx.x * kChunk + threadIdx.x;
+  if (t < T) {
+    const uint32_t bit = 1u << (threadIdx.x & 31);
+    const int word = threadIdx.x >> 5;
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(idx + static_cast<size_t>(t) * k + j);
+      if (e < 0 || e >= E) {
+        if (check) set_flag(err_flag, MOE_FLAG_BAD_EXPERT);
+        continue;
+      }
+      const uint32_t old = atomicOr(&bits[e * 8 + word], bit);
+      if (check && (old & bit)) set_flag(err_flag, MOE_FLAG_BAD_EXPERT);  // repeated id
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kChunk) chunk_hist_kernel(const int* __restrict__ idx, int T,
+                                                            int E, int k, int* __restrict__ hist,
+                                                            int* err_flag) {
+  extern __shared__ uint32_t bits[];
+  build_bits(bits, idx, T, E, k, err_flag, true);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int wd = 0; wd < 8; ++wd) c += __popc(bits[e * 8 + wd]);
+    hist[static_cast<size_t>(blockIdx.x) * E + e] = c;
+  }
+}
+
+// Inclusive block scan of one int per thread (blockDim.x == 1024).
+__device__ __forceinline__ int block_inclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_sums[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, s, o);
+      if (lane >= o) s += n;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int r = v + (wid > 0 ? warp_sums[wid - 1] : 0);
+  if (total) *total = warp_sums[31];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(int* __restrict__ hist, int nchunks, int E,
+                                                    long long rows_cap, int* __restrict__ counts,
+                                                    int* __restrict__ offsets,
+                                                    int* __restrict__ tile_sched,
+                                                    int* __restrict__ token_of) {
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = hist[static_cast<size_t>(c) * E + e];
+      hist[static_cast<size_t>(c) * E + e] = cnt;
+      cnt += v;
+    }
+    counts[e] = cnt;
+  }
+  const int tiles = (cnt + 127) >> 7;
+  int rows_total = 0, tiles_total = 0;
+  const int off = block_inclusive_scan(cnt, warp_sums, &rows_total) - cnt;
+  const int ts = block_inclusive_scan(tiles, warp_sums, &tiles_total) - tiles;
+  if (e < E) {
+    offsets[e] = off;
+    tile_sched[e] = ts;
+    for (int c = 0; c < nchunks; ++c) hist[static_cast<size_t>(c) * E + e] += off;
+  }
+  if (e == 0) {
+    offsets[E] = rows_total;
+    tile_sched[E] = tiles_total;
+  }
+  // rows never filled (only when bad ids were dropped) point at no token
+  for (long long r = rows_total + e; r < rows_cap; r += blockDim.x) token_of[r] = -1;
+}
+
+__global__ void __launch_bounds__(kChunk) maps_kernel(const int* __restrict__ idx, int T, int E,
+                                                      int k, const int* __restrict__ base,
+                                                      const float* __restrict__ topk_w,
+                                                      int* __restrict__ slot_of,
+                                                      int* __restrict__ token_of,
+                                                      float* __restrict__ row_w) {
+  extern __shared__ uint32_t bits[];
+  build_bits(bits, idx, T, E, k, nullptr, false);
+  const int t = blockIdx.x * kChunk + threadIdx.x;
+  if (t >= T) return;
+  const int word = threadIdx.x >> 5;
+  const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const size_t o = static_cast<size_t>(t) * k + j;
+    const int e = __ldg(idx + o);
+    if (e < 0 || e >= E) {
+      slot_of[o] = -1;
+      continue;
+    }
+    int rank = __popc(bits[e * 8 + word] & below);
+    for (int wd = 0; wd < word; ++wd) rank += __popc(bits[e * 8 + wd]);
+    const int slot = __ldg(base + static_cast<size_t>(blockIdx.x) * E + e) + rank;
+    slot_of[o] = slot;
+    token_of[slot] = t;
+    if (row_w) row_w[slot] = __ldg(topk_w + o);
+  }
+}
+
+// One warp per destination row; l/8 16-byte vectors per row.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
+                                                          const int* __restrict__ index,
+                                                          long long R, int nvec,
+                                                          uint4* __restrict__ dst) {
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
+  for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < R;
+       r += nwarps) {
+    const int t = __ldg(index + r);
+    uint4* d = dst + r * nvec;
+    if (t < 0) {
+      for (int v = lane; v < nvec; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* s = src + static_cast<long long>(t) * nvec;
+#pragma unroll 4
+    for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
+  }
+}
+
+// One warp per token; each lane owns up to 4 16-byte column vectors per pass.
+__global__ void __launch_bounds__(256) gather_sum_kernel(const uint4* __restrict__ src,
+                                                         const int* __restrict__ slot, int k,
+                                                         const uint4* __restrict__ add, int T,
+                                                         int nvec, uint4* __restrict__ out,
+                                                         long long ld_out_vec) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  for (int v0 = 0; v0 < nvec; v0 += 128) {
+    float acc[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int r = __ldg(slot + static_cast<size_t>(t) * k + j);
+      if (r < 0) continue;
+      const uint4* s = src + static_cast<long long>(r) * nvec;
+      uint4 x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int v = v0 + lane + 32 * i;
+        x[i] = (v < nvec) ? __ldg(s + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t wv[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[i][2 * e] += bf16_lo(wv[e]);
+          acc[i][2 * e + 1] += bf16_hi(wv[e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int v = v0 + lane + 32 * i;
+      if (v >= nvec) continue;
+      if (add) {
+        const uint4 a = __ldg(add + static_cast<long long>(t) * nvec + v);
+        const uint32_t wv[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[i][2 * e] += bf16_lo(wv[e]);
+          acc[i][2 * e + 1] += bf16_hi(wv[e]);
+        }
+      }
+      out[static_cast<long long>(t) * ld_out_vec + v] =
+          make_uint4(pack_bf16(acc[i][0], acc[i][1]), pack_bf16(acc[i][2], acc[i][3]),
+                     pack_bf16(acc[i][4], acc[i][5]), pack_bf16(acc[i][6], acc[i][7]));
+    }
+  }
+}
+
+__global__ void dw_reduce_kernel(const float* __restrict__ part, int nparts, long long R,
+                                 float* __restrict__ out) {
+  for (long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; r < R;
+       r += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float s = 0.0f;
+    for (int p = 0; p < nparts; ++p) s += part[r * nparts + p];
+    out[r] = s;
+  }
+}
+
+// One warp per token (k <= 32): dL[t][:] = 0 except dL[t][idx_j] = ds_j s_j (1 - s_j).
+__global__ void __launch_bounds__(256) router_bwd_kernel(
+    const float* __restrict__ d_row_w, const int* __restrict__ slot_of,
+    const int* __restrict__ topk_idx, const float* __restrict__ topk_w,
+    const float* __restrict__ topk_s, int T, int E, int k, float* __restrict__ d_topk_w,
+    bf16* __restrict__ dL, int* err_flag) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const size_t o = static_cast<size_t>(t) * k + lane;
+  float dw = 0.0f, w = 0.0f, s = 0.0f;
+  int e = -1;
+  if (lane < k) {
+    const int slot = __ldg(slot_of + o);
+    dw = slot >= 0 ? __ldg(d_row_w + slot) : 0.0f;
+    w = __ldg(topk_w + o);
+    s = __ldg(topk_s + o);
+    e = __ldg(topk_idx + o);
+    if (d_topk_w) d_topk_w[o] = dw;
+  }
+  float ssum = s, dS = w * dw;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, off);
+    dS += __shfl_xor_sync(0xFFFFFFFFu, dS, off);
+  }
+  bf16* row = dL + static_cast<size_t>(t) * E;
+  uint4* row4 = reinterpret_cast<uint4*>(row);
+  for (int v = lane; v < E / 8; v += 32) row4[v] = make_uint4(0, 0, 0, 0);
+  __syncwarp();
+  if (lane < k) {
+    if (e >= 0 && e < E) {
+      const float ds = (dw - dS) / ssum;
+      row[e] = __float2bfloat16_rn(ds * s * (1.0f - s));
+    } else {
+      set_flag(err_flag, MOE_FLAG_BAD_EXPERT);
+    }
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+
+cudaError_t launch_topk(const float* L, const float* bias, int T, int E, int k, int* idx,
+                        float* w, float* s, int* err_flag, cudaStream_t st) {
+  const int grid = (T + 7) / 8;
+  const int npl = (E + 31) / 32;
+  LaunchTimer lt("topk_sigmoid", st);
+  if (npl <= 2) topk_sigmoid_kernel<2><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
+  else if (npl <= 4) topk_sigmoid_kernel<4><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
+  else if (npl <= 8) topk_sigmoid_kernel<8><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
+  else if (npl <= 16) topk_sigmoid_kernel<16><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
+  else if (npl <= 28) topk_sigmoid_kernel<28><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
+  else topk_sigmoid_kernel<32><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
+  return cudaGetLastError();
+}
+
+int permute_chunks(int T) { return (T + kChunk - 1) / kChunk; }
+
+cudaError_t launch_permute_maps(const int* idx, const float* topk_w, int T, int E, int k,
+                                int* hist_ws, int* counts, int* offsets, int* slot_of,
+                                int* token_of, int* tile_sched, float* row_w, int* err_flag,
+                                cudaStream_t st) {
+  const int nch = permute_chunks(T);
+  const size_t sm = static_cast<size_t>(E) * 8 * sizeof(uint32_t);
+  {
+    LaunchTimer lt("permute_hist", st);
+    chunk_hist_kernel<<<nch, kChunk, sm, st>>>(idx, T, E, k, hist_ws, err_flag);
+  }
+  {
+    LaunchTimer lt("permute_scan", st);
+    scan_kernel<<<1, 1024, 0, st>>>(hist_ws, nch, E, static_cast<long long>(T) * k, counts,
+                                    offsets, tile_sched, token_of);
+  }
+  {
+    LaunchTimer lt("permute_maps", st);
+    maps_kernel<<<nch, kChunk, sm, st>>>(idx, T, E, k, hist_ws, topk_w, slot_of, token_of, row_w);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const char* name, const void* src, const int* index, long long R,
+                               int l, void* dst, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  const long long warps = R;
+  long long blocks = (warps + 7) / 8;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  LaunchTimer lt(name, st);
+  gather_rows_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(src), index, R, l / 8, reinterpret_cast<uint4*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_sum(const char* name, const void* src, const int* slot, int k,
+                              const void* add, int T, int l, void* out, long long ld_out,
+                              cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  LaunchTimer lt(name, st);
+  gather_sum_kernel<<<(T + 7) / 8, 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(src), slot, k, reinterpret_cast<const uint4*>(add), T, l / 8,
+      reinterpret_cast<uint4*>(out), ld_out / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_reduce(const float* part, int nparts, long long R, float* out,
+                             cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  long long blocks = (R + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  LaunchTimer lt("routing_weight_grad_reduce", st);
+  dw_reduce_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(part, nparts, R, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd(const float* d_row_w, const int* slot_of, const int* topk_idx,
+                              const float* topk_w, const float* topk_s, int T, int E, int k,
+                              float* d_topk_w, void* dL, int* err_flag, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  LaunchTimer lt("router_bwd_dlogits", st);
+  router_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(d_row_w, slot_of, topk_idx, topk_w, topk_s, T, E,
+                                                 k, d_topk_w, reinterpret_cast<bf16*>(dL),
+                                                 err_flag);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,136 @@
+"""The LatentMoE layer as a sequence of libmoe calls (forward and backward).
+
+PyTorch only provides the device buffers and the stream; every step runs in a
+libmoe CUDA kernel. One instance holds all activations, workspaces and weight
+gradients for a fixed token count T, so a step allocates nothing.
+
+Forward  (loss-free):  route_topk -> latent_proj(down) -> permute ->
+         grouped_swiglu -> shared_swiglu -> unpermute_combine -> latent_proj(up)
+Backward (dout given): latent_proj_bwd(up) -> unpermute_combine_bwd ->
+         grouped_swiglu_bwd -> shared_swiglu_bwd -> permute_bwd ->
+         latent_proj_bwd(down) -> route_topk_bwd (adds the router's dx)
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as M
+
+BF16 = torch.bfloat16
+
+
+class LatentMoELayer:
+    def __init__(self, weights: dict, T: int, k: int, wgrad_dtype: int = M.MOE_DTYPE_F32,
+                 device="cuda"):
+        self.w = weights
+        self.T = T
+        self.k = k
+        self.d, self.E = weights["Wr"].shape
+        self.l = weights["W_dn"].shape[1]
+        self.f = weights["W2"].shape[1]
+        self.S = weights["W13_sh"].shape[0]
+        self.R = T * k
+        self.wgrad_dtype = wgrad_dtype
+        dev = torch.device(device)
+        T_, k_, d, l, f, E, S, R = T, k, self.d, self.l, self.f, self.E, self.S, self.R
+        e = lambda *shape, dt=BF16: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
+        wdt = torch.float32 if wgrad_dtype == M.MOE_DTYPE_F32 else BF16
+        # forward activations
+        self.topk_idx = e(T_, k_, dt=torch.int32)
+        self.topk_w = e(T_, k_, dt=torch.float32)
+        self.topk_s = e(T_, k_, dt=torch.float32)
+        self.z = e(T_, l)
+        self.counts = e(E, dt=torch.int32)
+        self.offsets = e(E + 1, dt=torch.int32)
+        self.tile_sched = e(E + 1, dt=torch.int32)
+        self.slot_of = e(T_, k_, dt=torch.int32)
+        self.token_of = e(R, dt=torch.int32)
+        self.row_w = e(R, dt=torch.float32)
+        self.z_perm = e(R, l)
+        self.gu = e(R, 2 * f)
+        self.h = e(R, f)
+        self.y_perm = e(R, l)
+        self.gu_sh = e(T_, S * 2 * f)
+        self.h_sh = e(T_, S * f)
+        self.y_sh = e(T_, l)
+        self.y_lat = e(T_, l)
+        self.out = e(T_, d)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        # backward
+        self.dy_lat = e(T_, l)
+        self.dy_perm = e(R, l)
+        self.dz_perm = e(R, l)
+        self.d_row_w = e(R, dt=torch.float32)
+        self.d_topk_w = e(T_, k_, dt=torch.float32)
+        self.dz_sh = e(T_, l)
+        self.dz = e(T_, l)
+        self.dx = e(T_, d)
+        self.grads = {
+            "W_up": e(l, d, dt=wdt), "W_dn": e(d, l, dt=wdt), "Wr": e(d, E, dt=wdt),
+            "W13": e(E, l, 2 * f, dt=wdt), "W2": e(E, f, l, dt=wdt),
+            "W13_sh": e(S, l, 2 * f, dt=wdt), "W2_sh": e(S, f, l, dt=wdt),
+        }
+        # workspaces
+        ws = lambda op, **kw: M.moe_workspace_size(op, **kw)  # noqa: E731
+        self.ws_sizes = {
+            "route": ws(M.MOE_OP_ROUTE_TOPK, T=T_, E=E),
+            "permute": ws(M.MOE_OP_PERMUTE, T=T_, E=E),
+            "gbwd": ws(M.MOE_OP_GROUPED_SWIGLU_BWD, T=R, k=1, f=f),
+            "sbwd": ws(M.MOE_OP_SHARED_SWIGLU_BWD, T=T_, f=f, S=S),
+            "rbwd": ws(M.MOE_OP_ROUTE_TOPK_BWD, T=T_, E=E),
+        }
+        self.ws = {n: torch.empty(max(b, 256), dtype=torch.uint8, device=dev)
+                   for n, b in self.ws_sizes.items()}
+
+    # ------------------------------------------------------------------ forward
+    def forward(self, x, stream=None):
+        w, T, k, d, l, f, E, S, R = (self.w, self.T, self.k, self.d, self.l, self.f, self.E,
+                                     self.S, self.R)
+        self.x = x
+        M.moe_route_topk(x, w["Wr"], w.get("bias"), T, d, E, k, self.topk_idx, self.topk_w,
+                         self.topk_s, self.ws["route"], self.ws_sizes["route"], self.err, stream)
+        M.moe_latent_proj(x, w["W_dn"], T, d, l, self.z, stream)
+        M.moe_permute(self.z, self.topk_idx, self.topk_w, T, l, E, k, self.z_perm, self.counts,
+                      self.offsets, self.slot_of, self.token_of, self.tile_sched, self.row_w,
+                      self.ws["permute"], self.ws_sizes["permute"], self.err, stream)
+        M.moe_grouped_swiglu(self.z_perm, w["W13"], w["W2"], self.offsets, self.tile_sched,
+                             self.row_w, E, R, l, f, self.gu, self.h, self.y_perm, stream)
+        M.moe_shared_swiglu(self.z, w["W13_sh"], w["W2_sh"], T, l, f, S, self.gu_sh, self.h_sh,
+                            self.y_sh, stream)
+        M.moe_unpermute_combine(self.y_perm, self.slot_of, self.y_sh, T, k, l, self.y_lat, stream)
+        M.moe_latent_proj(self.y_lat, w["W_up"], T, l, d, self.out, stream)
+        return self.out
+
+    # ------------------------------------------------------------------ backward
+    def backward(self, dout, stream=None):
+        w, T, k, d, l, f, E, S, R = (self.w, self.T, self.k, self.d, self.l, self.f, self.E,
+                                     self.S, self.R)
+        g = self.grads
+        wd = self.wgrad_dtype
+        M.moe_latent_proj_bwd(dout, self.y_lat, w["W_up"], T, l, d, self.dy_lat, g["W_up"], wd,
+                              stream)
+        M.moe_unpermute_combine_bwd(self.dy_lat, self.token_of, T, k, l, self.dy_perm, stream)
+        M.moe_grouped_swiglu_bwd(self.dy_perm, self.z_perm, w["W13"], w["W2"], self.gu, self.h,
+                                 self.row_w, self.offsets, self.tile_sched, E, R, l, f,
+                                 self.dz_perm, self.d_row_w, g["W13"], g["W2"], wd,
+                                 self.ws["gbwd"], self.ws_sizes["gbwd"], stream)
+        M.moe_shared_swiglu_bwd(self.dy_lat, self.z, w["W13_sh"], w["W2_sh"], self.gu_sh,
+                                self.h_sh, T, l, f, S, self.dz_sh, g["W13_sh"], g["W2_sh"], wd,
+                                self.ws["sbwd"], self.ws_sizes["sbwd"], stream)
+        M.moe_permute_bwd(self.dz_perm, self.slot_of, self.dz_sh, T, k, l, self.dz, stream)
+        M.moe_latent_proj_bwd(self.dz, self.x, w["W_dn"], T, d, l, self.dx, g["W_dn"], wd, stream)
+        M.moe_route_topk_bwd(self.d_row_w, self.slot_of, self.topk_idx, self.topk_w, self.topk_s,
+                             self.x, w["Wr"], T, d, E, k, self.d_topk_w, self.dx, g["Wr"], wd,
+                             self.ws["rbwd"], self.ws_sizes["rbwd"], self.err, stream)
+        return self.dx
+
+    def step(self, x, dout, stream=None):
+        self.forward(x, stream)
+        return self.backward(dout, stream)
+
+
+def weights_to_device(inp: dict, device="cuda") -> dict:
+    names = ("Wr", "W_dn", "W13", "W2", "W13_sh", "W2_sh", "W_up")
+    out = {n: inp[n].to(device) for n in names}
+    out["bias"] = inp["bias"].to(device) if inp.get("bias") is not None else None
+    return out

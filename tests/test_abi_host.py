@@ -1,0 +1,76 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads
+and exports every entry point include/moe.h declares; the binding covers them
+with the right arity; argument errors are reported before any CUDA call."""
+import os
+import re
+
+import pytest
+
+from sparse_moe_layer_topk_gb300 import _lib as M
+from sparse_moe_layer_topk_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "moe.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    decls = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?[\w\s\*]+?\b(moe_\w+)\s*\(([^)]*)\)\s*;", txt, re.M):
+        args = [a for a in m.group(2).split(",") if a.strip() and a.strip() != "void"]
+        decls[m.group(1)] = len(args)
+    return decls
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build_library()
+    return M.load()
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    decls = _declared()
+    assert len(decls) >= 18
+    for name, nargs in decls.items():
+        assert hasattr(lib, name), name
+        assert name in M.SIGNATURES, name
+        assert len(M.SIGNATURES[name][0]) == nargs, (name, nargs)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.moe_version() >= 1
+    for code in (M.MOE_OK, M.MOE_ERR_ARG, M.MOE_ERR_ALIGN, M.MOE_ERR_WORKSPACE,
+                 M.MOE_ERR_UNSUPPORTED, M.MOE_ERR_CUDA):
+        assert lib.moe_status_string(code)
+
+
+def test_workspace_sizes(lib):
+    assert M.moe_workspace_size(M.MOE_OP_ROUTE_TOPK, T=4096, E=896) >= 4096 * 896 * 4
+    assert M.moe_workspace_size(M.MOE_OP_PERMUTE, T=4096, E=896) >= 16 * 896 * 4
+    # the SwiGLU-backward row partials need at least one slot per row even for f < 128
+    assert M.moe_workspace_size(M.MOE_OP_GROUPED_SWIGLU_BWD, T=100, k=1, f=64) >= \
+        100 * (2 * 64 * 2 + 64 * 2 + 4)
+    assert M.moe_workspace_size(M.MOE_OP_ROUTE_TOPK_BWD, T=10, E=64) >= 10 * 64 * 2
+
+
+def test_argument_errors_before_any_cuda_call(lib):
+    P = 0x1000
+    # null pointers
+    assert lib.moe_latent_proj(None, None, 4, 64, 64, None, None) == M.MOE_ERR_ARG
+    # dimension not a multiple of 64
+    assert lib.moe_latent_proj(P, P, 4, 64, 96, P, None) == M.MOE_ERR_ALIGN
+    # misaligned pointer
+    assert lib.moe_latent_proj(P + 2, P, 4, 64, 64, P, None) == M.MOE_ERR_ALIGN
+    # k out of range, E too large
+    assert lib.moe_topk_from_logits(P, None, 4, 64, 33, P, P, P, None, None) == M.MOE_ERR_ARG
+    assert lib.moe_topk_from_logits(P, None, 4, 2048, 4, P, P, P, None, None) == M.MOE_ERR_ARG
+    # workspace too small
+    assert lib.moe_route_topk(P, P, None, 64, 64, 64, 4, P, P, P, P, 16, None, None) == \
+        M.MOE_ERR_WORKSPACE
+    assert lib.moe_permute(None, P, None, 64, 64, 64, 4, None, P, P, P, P, P, None, P, 8, None,
+                           None) == M.MOE_ERR_WORKSPACE
+    # backward without the saved gate/up activations is not supported
+    assert lib.moe_grouped_swiglu_bwd(P, P, P, P, None, P, P, P, P, 8, 64, 64, 64, P, P, P, P, 0,
+                                      P, 1 << 30, None) == M.MOE_ERR_UNSUPPORTED
+    # bad wgrad dtype
+    assert lib.moe_latent_proj_bwd(P, P, P, 4, 64, 64, None, P, 7, None) == M.MOE_ERR_ARG

@@ -1,0 +1,196 @@
+"""Whole-layer parity of the libmoe forward/backward sequence against the fp64
+oracle, on the seeded workloads (GPU).
+
+Routing: the GPU decides on fp32 logits, the oracle on exact ones, so a token
+whose k-th and (k+1)-th logits are closer than the fp32 rounding can pick a
+different last expert. Such tokens must be rare and near-ties (oracle gap
+< 1e-3); they are excluded from the per-token comparisons, and experts that
+received a disagreeing token are excluded from the per-expert ones. Everything
+else is compared with the bf16 I/O tolerances (max-abs 2e-2, relative
+Frobenius 1e-2; weight gradients: max-abs relative to max|ref|)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from sparse_moe_layer_topk_gb300 import _lib as M
+from sparse_moe_layer_topk_gb300 import inputs as I
+from sparse_moe_layer_topk_gb300.layer import LatentMoELayer, weights_to_device
+
+from gpu_util import check_close, f64, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+GRAD_NAMES = {"Wr": "dWr", "W_dn": "dW_dn", "W13": "dW13", "W2": "dW2", "W13_sh": "dW13_sh",
+              "W2_sh": "dW2_sh", "W_up": "dW_up"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _run(inp, T=None, wgrad=M.MOE_DTYPE_F32, backward=True):
+    cfg = inp["cfg"]
+    T = inp["x"].shape[0] if T is None else T
+    layer = LatentMoELayer(weights_to_device(inp), T, cfg.k, wgrad)
+    layer.forward(inp["x"].cuda())
+    if backward:
+        layer.backward(inp["g"].cuda())
+    torch.cuda.synchronize()
+    assert int(layer.err.item()) == 0
+    return layer
+
+
+def _routing_disagreement(layer, L_ref, k):
+    """Tokens whose GPU selection differs from the oracle's; each must be a near-tie."""
+    gi = layer.topk_idx.cpu().numpy()
+    ri = O.topk_select(L_ref, k)
+    bad = np.where((np.sort(gi, 1) != np.sort(ri, 1)).any(1))[0]
+    if bad.size:
+        Ls = -np.sort(-L_ref[bad], axis=1)
+        gaps = Ls[:, k - 1] - Ls[:, k]
+        assert np.all(gaps < 1e-3), gaps
+    return bad, ri
+
+
+def test_layer_cfg0_forward_backward_all_outputs():
+    inp = I.make_layer_inputs(0)
+    cfg = inp["cfg"]
+    layer = _run(inp)
+    fwd = O.layer_forward(inp)
+    bwd = O.layer_backward(inp, fwd)
+    bad, _ = _routing_disagreement(layer, fwd["L"], cfg.k)
+    assert bad.size == 0
+    np.testing.assert_array_equal(layer.counts.cpu().numpy(), fwd["counts"])
+    np.testing.assert_array_equal(layer.offsets.cpu().numpy(), fwd["offsets"])
+    np.testing.assert_array_equal(layer.slot_of.cpu().numpy(), fwd["slot_of"])
+    np.testing.assert_array_equal(layer.token_of.cpu().numpy(), fwd["token_of"])
+    check_close("w", f64(layer.topk_w), fwd["w"], max_abs=1e-5, rel_fro=1e-5)
+    for name in ("z", "y_lat", "out"):
+        check_close(name, f64(getattr(layer, name)), fwd[name])
+    check_close("z_perm", f64(layer.z_perm), fwd["z_perm"])
+    check_close("dx", f64(layer.dx), bwd["dx"])
+    check_close("d_w", f64(layer.d_topk_w), bwd["d_w"])
+    for wn, gn in GRAD_NAMES.items():
+        check_close(gn, f64(layer.grads[wn]), bwd[gn], scale_by_max=True)
+
+
+def test_layer_cfg0_bf16_wgrad():
+    inp = I.make_layer_inputs(0)
+    layer = _run(inp, wgrad=M.MOE_DTYPE_BF16)
+    fwd = O.layer_forward(inp)
+    bwd = O.layer_backward(inp, fwd)
+    for wn, gn in GRAD_NAMES.items():
+        assert layer.grads[wn].dtype == torch.bfloat16
+        check_close(gn, f64(layer.grads[wn]), bwd[gn], scale_by_max=True)
+
+
+def test_layer_ragged_token_count():
+    """T not a multiple of any tile (ragged tails everywhere), cfg0 widths."""
+    inp = I.make_layer_inputs(0, T=77)
+    layer = _run(inp)
+    fwd = O.layer_forward(inp)
+    bwd = O.layer_backward(inp, fwd)
+    bad, _ = _routing_disagreement(layer, fwd["L"], inp["cfg"].k)
+    assert bad.size == 0
+    check_close("out", f64(layer.out), fwd["out"])
+    check_close("dx", f64(layer.dx), bwd["dx"])
+    for wn, gn in GRAD_NAMES.items():
+        check_close(gn, f64(layer.grads[wn]), bwd[gn], scale_by_max=True)
+
+
+def test_layer_single_token():
+    inp = I.make_layer_inputs(0, T=1)
+    layer = _run(inp)
+    fwd = O.layer_forward(inp)
+    bwd = O.layer_backward(inp, fwd)
+    check_close("out", f64(layer.out), fwd["out"])
+    check_close("dx", f64(layer.dx), bwd["dx"])
+    check_close("dW13", f64(layer.grads["W13"]), bwd["dW13"], scale_by_max=True)
+    # all but k experts are empty: their gradients are exact zeros
+    empty = np.where(fwd["counts"] == 0)[0]
+    assert not layer.grads["W13"][empty].any() and not layer.grads["W2"][empty].any()
+
+
+@pytest.mark.parametrize("cfg_id", [1, 2])
+def test_layer_full_size_forward(cfg_id):
+    inp = I.make_layer_inputs(cfg_id)
+    cfg = inp["cfg"]
+    layer = _run(inp, backward=False)
+    fwd = O.layer_forward(inp)
+    bad, _ = _routing_disagreement(layer, fwd["L"], cfg.k)
+    assert bad.size <= max(2, cfg.T // 1000), bad.size
+    keep = np.setdiff1d(np.arange(cfg.T), bad)
+    check_close("out", f64(layer.out)[keep], fwd["out"][keep])
+    check_close("y_lat", f64(layer.y_lat)[keep], fwd["y_lat"][keep])
+    if bad.size == 0:
+        np.testing.assert_array_equal(layer.counts.cpu().numpy(), fwd["counts"])
+        np.testing.assert_array_equal(layer.slot_of.cpu().numpy(), fwd["slot_of"])
+    if cfg.skew:
+        counts = layer.counts.cpu().numpy()
+        assert (counts <= 2).sum() >= 150 and (counts == 0).sum() > 0
+
+
+def test_ep_rank_grouped_gemm_and_return():
+    """One expert-parallel rank: 14 experts over 65536 pre-permuted rows, then
+    the weighted return to arrival order (combine with k = 1)."""
+    inp = I.make_ep_rank_inputs()
+    cfg = inp["cfg"]
+    counts = inp["counts"].numpy()
+    offsets = O.expert_offsets(counts)
+    sched = O.m_tiles_schedule(counts, 128)
+    R, l, f, E = cfg.R, cfg.l, cfg.f, cfg.E
+    gu = torch.empty(R, 2 * f, dtype=torch.bfloat16, device="cuda")
+    h = torch.empty(R, f, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(R, l, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(R, l, dtype=torch.bfloat16, device="cuda")
+    M.moe_grouped_swiglu(inp["z_perm"].cuda(), inp["W13"].cuda(), inp["W2"].cuda(),
+                         torch.from_numpy(offsets).int().cuda(), torch.from_numpy(sched).int().cuda(),
+                         inp["w"].cuda(), E, R, l, f, None, h, y)
+    perm = inp["perm"].numpy()
+    inv = np.empty(R, dtype=np.int32)
+    inv[perm] = np.arange(R, dtype=np.int32)        # slot of arrival row t
+    M.moe_unpermute_combine(y, torch.from_numpy(inv).reshape(R, 1).cuda(), None, R, 1, l, out)
+    torch.cuda.synchronize()
+    ref = O.ep_rank_forward(inp["z_perm"], counts, inp["W13"], inp["W2"], inp["w"], perm)
+    check_close("ep_out", f64(out), ref)
+
+
+def test_layer_fwd_bwd_T16384_sampled():
+    """The benchmark workload at full size (T=16384): every output and input
+    gradient of sampled tokens, and the expert weight gradients of sampled
+    experts, against the oracle run on exactly the tokens they depend on; the
+    dense weight gradients against their defining products of the layer's
+    own activations."""
+    inp = I.make_layer_inputs(4)
+    cfg = inp["cfg"]
+    layer = _run(inp)
+    L = O.router_logits(inp["x"], inp["Wr"], inp["bias"])
+    bad, ref_idx = _routing_disagreement(layer, L, cfg.k)
+    assert bad.size <= 20, bad.size
+    rng = np.random.default_rng(0)
+    toks = np.setdiff1d(rng.choice(cfg.T, 96, replace=False), bad)
+    sub = dict(inp)
+    sub["x"], sub["g"] = inp["x"][toks], inp["g"][toks]
+    fwd = O.layer_forward(sub)
+    bwd = O.layer_backward(sub, fwd)
+    check_close("out", f64(layer.out)[toks], fwd["out"])
+    check_close("dx", f64(layer.dx)[toks], bwd["dx"])
+    # sampled experts whose token set is the same on both sides
+    gpu_idx = layer.topk_idx.cpu().numpy()
+    touched = set(np.unique(gpu_idx[bad])) | set(np.unique(ref_idx[bad]))
+    cand = [e for e in rng.permutation(cfg.E) if e not in touched][:6]
+    for e in cand:
+        te = np.where((ref_idx == e).any(1))[0]
+        sub = dict(inp)
+        sub["x"], sub["g"] = inp["x"][te], inp["g"][te]
+        fe = O.layer_forward(sub)
+        be = O.layer_backward(sub, fe)
+        check_close(f"dW13[{e}]", f64(layer.grads["W13"][e]), be["dW13"][e], scale_by_max=True)
+        check_close(f"dW2[{e}]", f64(layer.grads["W2"][e]), be["dW2"][e], scale_by_max=True)
+    # dense weight gradients = their defining products on the layer's activations
+    check_close("dW_up", f64(layer.grads["W_up"]), f64(layer.y_lat).T @ f64(inp["g"]),
+                scale_by_max=True)
+    check_close("dW_dn", f64(layer.grads["W_dn"]), f64(inp["x"]).T @ f64(layer.dz),
+                scale_by_max=True)
