@@ -240,7 +240,8 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
  * objects are created on first use and reused). moe_timing_report, called
  * after the caller synchronised those streams, writes one line per kernel
  * label, "label launches total_ms", into buf (NUL-terminated, truncated to
- * len), forgets the recorded pairs and returns the length of the full text. */
+ * len), forgets the recorded pairs and returns the length of the full text.
+ * With buf == NULL it only returns that length and keeps the pairs. */
 int moe_timing_enable(int on);
 int moe_timing_report(char* buf, size_t len);
 

@@ -71,10 +71,14 @@ int moe_timing_report(char* buf, size_t len) {
       slot.first += 1;
       slot.second += ms;
     }
-    moe::g_free.push_back(p.a);
-    moe::g_free.push_back(p.b);
   }
-  moe::g_pairs.clear();
+  if (buf) {  // a report into a buffer consumes the recorded pairs
+    for (auto& p : moe::g_pairs) {
+      moe::g_free.push_back(p.a);
+      moe::g_free.push_back(p.b);
+    }
+    moe::g_pairs.clear();
+  }
   std::string out;
   char line[256];
   for (auto& kv : acc) {

@@ -125,8 +125,19 @@ def test_layer_full_size_forward(cfg_id):
     check_close("out", f64(layer.out)[keep], fwd["out"][keep])
     check_close("y_lat", f64(layer.y_lat)[keep], fwd["y_lat"][keep])
     if bad.size == 0:
+        # same expert sets: counts, offsets and each token's expert -> slot map
+        # are unique; the order of a token's experts may differ where two of its
+        # selected logits are closer than the fp32 rounding
         np.testing.assert_array_equal(layer.counts.cpu().numpy(), fwd["counts"])
-        np.testing.assert_array_equal(layer.slot_of.cpu().numpy(), fwd["slot_of"])
+        np.testing.assert_array_equal(layer.offsets.cpu().numpy(), fwd["offsets"])
+        gi, gs = layer.topk_idx.cpu().numpy(), layer.slot_of.cpu().numpy()
+        og, os_ = np.argsort(gi, 1), np.argsort(fwd["idx"], 1)
+        np.testing.assert_array_equal(np.take_along_axis(gs, og, 1),
+                                      np.take_along_axis(fwd["slot_of"], os_, 1))
+        reordered = np.where((gi != fwd["idx"]).any(1))[0]
+        for t in reordered:
+            Lsel = fwd["L"][t, fwd["idx"][t]]
+            assert np.min(np.abs(np.diff(np.sort(Lsel)))) < 1e-3
     if cfg.skew:
         counts = layer.counts.cpu().numpy()
         assert (counts <= 2).sum() >= 150 and (counts == 0).sum() > 0
