@@ -130,6 +130,23 @@ int moe_permute(const uint16_t* z, const int32_t* topk_idx, const float* topk_w,
                 int32_t* slot_of, int32_t* token_of, int32_t* tile_sched, float* row_w,
                 void* ws, size_t ws_bytes, int32_t* err_flag, void* stream);
 
+/* Allocation-free variant of moe_permute, for callers that cannot allocate
+ * device memory (a caller that is handed only its input and output buffers,
+ * or one on a fixed memory budget that must not call cudaMalloc/cudaFree,
+ * which may also synchronise the device). The pages describe nothing like it;
+ * it computes exactly what moe_permute computes, with the same arguments
+ * except ws / ws_bytes. Its scratch is a fixed 1 MiB array inside the library
+ * (held on every GPU that loads the library until it is unloaded), so it
+ * handles permute_chunks(T) * E <= 262144, i.e. ceil(T / 256) * E <= 262144
+ * (T <= 74,752 at E = 896); larger problems return MOE_ERR_WORKSPACE without
+ * launching anything. The first call on a device looks up the array's device
+ * address; make that first call before any stream capture. All calls share the
+ * array: calls that may overlap on the GPU must be serialised by the caller. */
+int moe_permute_noalloc(const uint16_t* z, const int32_t* topk_idx, const float* topk_w, int T,
+                        int l, int E, int k, uint16_t* z_perm, int32_t* counts, int32_t* offsets,
+                        int32_t* slot_of, int32_t* token_of, int32_t* tile_sched, float* row_w,
+                        int32_t* err_flag, void* stream);
+
 /* ---------------------------------------------------------------- projections */
 
 /* Latent projection of [MODEL]: out[M][N] (bf16) = in[M][K] @ W[K][N] (bf16,

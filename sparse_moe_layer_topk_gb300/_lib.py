@@ -45,6 +45,7 @@ SIGNATURES = {
     "moe_topk_from_logits": ([_P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_route_topk": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P, _P], _I),
     "moe_permute": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P], _I),
+    "moe_permute_noalloc": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_latent_proj": ([_P, _P, _I, _I, _I, _P, _P], _I),
     "moe_latent_proj_bwd": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P], _I),
     "moe_grouped_swiglu": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
@@ -151,6 +152,14 @@ def moe_permute(z, topk_idx, topk_w, T, l, E, k, z_perm, counts, offsets, slot_o
                 tile_sched, row_w, ws, ws_bytes, err_flag=None, stream=None):
     _call("moe_permute", z, topk_idx, topk_w, T, l, E, k, z_perm, counts, offsets, slot_of,
           token_of, tile_sched, row_w, ws, ws_bytes, err_flag, stream)
+
+
+def moe_permute_noalloc(z, topk_idx, topk_w, T, l, E, k, z_perm, counts, offsets, slot_of,
+                        token_of, tile_sched, row_w, err_flag=None, stream=None):
+    """moe_permute without a workspace argument, for callers that cannot allocate
+    device memory; the scratch is a fixed array inside the library (see moe.h)."""
+    _call("moe_permute_noalloc", z, topk_idx, topk_w, T, l, E, k, z_perm, counts, offsets,
+          slot_of, token_of, tile_sched, row_w, err_flag, stream)
 
 
 def moe_latent_proj(inp, W, M, K, N, out, stream=None):
