@@ -21,6 +21,7 @@
 // "权重预取与梯度归约".
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -42,7 +43,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * 6144 + 1024 + 256;
 };
 
 struct Params {
@@ -68,6 +69,7 @@ struct Params {
   float* dw_part;
   int dw_nparts;
   int* err_flag;
+  int c0_rank3;  // the C store map is 3-D (grouped-K groups or column batches)
 };
 
 struct Tile {
@@ -316,17 +318,94 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
 }
 
 // ------------------------------------------------------------------ epilogue
+//
+// Each epilogue warp owns 32 accumulator rows (its TMEM lane quadrant) and
+// walks the tile in 32-column chunks. Full 32x32 output blocks are written to
+// the warp's swizzled staging area in shared memory and stored by one TMA
+// tensor store per block (64-byte swizzle for bf16 rows, 128-byte for fp32);
+// the staging area is reused once the previous chunk's stores have read it.
+// TMA clips rows and columns outside the output tensor; the only blocks that
+// take per-thread stores are the last, partial 32-row blocks of an expert
+// segment (rows past it belong to the next expert) and read-modify-write
+// accumulation.
+
+constexpr int STAGING_PER_WARP = 6144;  // three 2 KB bf16 blocks or one 4 KB fp32 block
 
 __device__ __forceinline__ void store16(void* dst, uint4 v) { *reinterpret_cast<uint4*>(dst) = v; }
 
+// Row `row` (= lane) of a 32x32 bf16 block: 64-byte rows, 64-byte TMA swizzle.
+__device__ __forceinline__ void stage_bf16(uint8_t* blk, int row, const float* v) {
+  uint8_t* rp = blk + row * 64;
+  const int sw = (row >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(rp + ((c ^ sw) << 4)) =
+        make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                   pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+}
+
+// Row `row` of a 32x32 fp32 block: 128-byte rows, 128-byte TMA swizzle.
+__device__ __forceinline__ void stage_f32(uint8_t* blk, int row, const float* v) {
+  uint8_t* rp = blk + row * 128;
+  const int sw = row & 7;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(rp + ((c ^ sw) << 4)) =
+        make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                   __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+}
+
+__device__ __forceinline__ void store_bf16_row(bf16* dst, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    store16(dst + 8 * c,
+            make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                       pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7])));
+}
+
+__device__ __forceinline__ void store_f32_row(float* dst, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    store16(dst + 4 * c, make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                                    __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3])));
+}
+
+__device__ __forceinline__ void ld_chunk(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct StoreMaps {
+  const CUtensorMap* c0;  // C / h / dgu
+  const CUtensorMap* c1;  // gu (SwiGLU) / w*h (SwiGLU backward)
+  int c0_rank3;
+};
+
 template <int BN>
-__device__ void epilogue_loop(const Params& p, uint64_t* tfull, uint64_t* tempty,
-                              uint32_t tmem_base, volatile int* abort_flag) {
+__device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* staging,
+                              uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base,
+                              volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5;
   const int q = warp & 3;  // tensor-memory lane quadrant this warp may read
   const uint32_t lane = lane_id();
   const int r_loc = q * 32 + static_cast<int>(lane);
+  uint8_t* stg = staging + (warp - 2) * STAGING_PER_WARP;
+  const uint32_t stg_s = smem_u32(stg);
   const int total = total_tiles(p);
+  bool pending = false;  // a bulk store of this warp may still read the staging area
+  auto stage_begin = [&]() {
+    if (pending) {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+    }
+  };
+  auto stage_end = [&]() {
+    fence_proxy_async_smem();
+    __syncwarp();
+  };
   int it = 0;
   for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
     const Tile ti = decode<BN>(p, t);
@@ -337,200 +416,214 @@ __device__ void epilogue_loop(const Params& p, uint64_t* tfull, uint64_t* tempty
       break;
     }
     tc_fence_after();
+    const int blk_rows = ti.rows - q * 32;  // valid rows of this warp's 32-row block
     const bool row_ok = r_loc < ti.rows;
     const long long grow = static_cast<long long>(ti.m0) + r_loc;
+    const int row0 = ti.m0 + q * 32;
     const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(buf * BN);
     const bool has_acc = ti.nk > 0;
+    // TMA clips outside the tensor; inside it (grouped-M) only full blocks may use it.
+    const bool use_tma = blk_rows >= 32 || p.sched != SCHED_GROUPED_M;
 
-    if (p.epi == EPI_STORE) {
+    if (blk_rows > 0) {
+      if (p.epi == EPI_STORE) {
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int n = ti.nb0 + c * 32;  // output column over the full N
-        if (n >= p.N) break;             // warp-uniform N tail
-        int ncol = n;
-        long long cbase = 0;
-        if (p.sched == SCHED_GROUPED_K) {
-          cbase = static_cast<long long>(ti.g) * p.c_batch_stride;
-        } else if (p.c_batch_n > 0) {
-          const int cb = n / p.c_batch_n;
-          ncol = n - cb * p.c_batch_n;
-          cbase = static_cast<long long>(cb) * p.c_batch_stride;
+        for (int c = 0; c < BN / 32; ++c) {
+          const int n = ti.nb0 + c * 32;
+          if (n >= p.N) break;  // warp-uniform N tail
+          float v[32];
+          if (has_acc) {
+            ld_chunk(trow + c * 32, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          }
+          int ncol = n, cb = 0;
+          if (p.sched == SCHED_GROUPED_K) {
+            cb = ti.g;
+          } else if (p.c_batch_n > 0) {
+            cb = n / p.c_batch_n;
+            ncol = n - cb * p.c_batch_n;
+          }
+          if (use_tma && !p.accumulate) {
+            stage_begin();
+            if (p.c_bf16) stage_bf16(stg, lane, v); else stage_f32(stg, lane, v);
+            stage_end();
+            if (lane == 0) {
+              if (sm.c0_rank3) tma_store_3d(sm.c0, stg_s, ncol, row0, cb);
+              else tma_store_2d(sm.c0, stg_s, ncol, row0);
+              bulk_commit();
+            }
+            pending = true;
+          } else if (row_ok) {
+            const long long off = static_cast<long long>(cb) * p.c_batch_stride + grow * p.ldc + ncol;
+            if (p.c_bf16) {
+              bf16* dst = reinterpret_cast<bf16*>(p.C) + off;
+              if (p.accumulate) {
+#pragma unroll
+                for (int vv = 0; vv < 4; ++vv) {
+                  const uint4 old = *reinterpret_cast<const uint4*>(dst + vv * 8);
+                  const uint32_t o[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    v[vv * 8 + 2 * e] += bf16_lo(o[e]);
+                    v[vv * 8 + 2 * e + 1] += bf16_hi(o[e]);
+                  }
+                }
+              }
+              store_bf16_row(dst, v);
+            } else {
+              store_f32_row(reinterpret_cast<float*>(p.C) + off, v);
+            }
+          }
         }
-        uint32_t r[32];
-        if (has_acc) {
-          tmem_ld_32x32b_x32(trow + c * 32, r);
-          tmem_ld_wait();
-        } else {
+      } else if (p.epi == EPI_SWIGLU) {
+        // TMEM columns [0, BN/2) hold the gate, [BN/2, BN) the up projection.
+        const int out_batch = (p.b_batch_mode == BATCH_FROM_N) ? ti.batch : 0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          float g[32], u[32], hv[32];
+          ld_chunk(trow + c * 32, g);
+          ld_chunk(trow + BN / 2 + c * 32, u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
+          for (int i = 0; i < 32; ++i) hv[i] = g[i] * sigmoidf_(g[i]) * u[i];
+          const int j = ti.nb0 + c * 32;
+          const int hcol = out_batch * p.f + j;
+          const int gcol = out_batch * 2 * p.f + j;
+          if (use_tma) {
+            stage_begin();
+            stage_bf16(stg, lane, hv);
+            if (p.gu) {
+              stage_bf16(stg + 2048, lane, g);
+              stage_bf16(stg + 4096, lane, u);
+            }
+            stage_end();
+            if (lane == 0) {
+              tma_store_2d(sm.c0, stg_s, hcol, row0);
+              if (p.gu) {
+                tma_store_2d(sm.c1, stg_s + 2048, gcol, row0);
+                tma_store_2d(sm.c1, stg_s + 4096, gcol + p.f, row0);
+              }
+              bulk_commit();
+            }
+            pending = true;
+          } else if (row_ok) {
+            store_bf16_row(p.h + grow * p.ldh + hcol, hv);
+            if (p.gu) {
+              store_bf16_row(p.gu + grow * p.ldgu + gcol, g);
+              store_bf16_row(p.gu + grow * p.ldgu + gcol + p.f, u);
+            }
+          }
         }
-        if (!row_ok) continue;
-        const long long off = cbase + grow * p.ldc + ncol;
-        if (p.c_bf16) {
-          bf16* dst = reinterpret_cast<bf16*>(p.C) + off;
-          if (p.accumulate) {
+      } else if (p.epi == EPI_ROWSCALE) {
+        const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int n = ti.nb0 + c * 32;
+          if (n >= p.N) break;
+          float v[32];
+          ld_chunk(trow + c * 32, v);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint4 old = *reinterpret_cast<const uint4*>(dst + v * 8);
-              const uint32_t o[4] = {old.x, old.y, old.z, old.w};
-              uint32_t pk[4];
+          for (int i = 0; i < 32; ++i) v[i] *= w;
+          if (use_tma) {
+            stage_begin();
+            stage_bf16(stg, lane, v);
+            stage_end();
+            if (lane == 0) {
+              tma_store_2d(sm.c0, stg_s, n, row0);
+              bulk_commit();
+            }
+            pending = true;
+          } else if (row_ok) {
+            store_bf16_row(reinterpret_cast<bf16*>(p.C) + grow * p.ldc + n, v);
+          }
+        }
+      } else {  // EPI_SWIGLU_BWD
+        const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
+        float dot = 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int n = ti.nb0 + c * 32;  // column of dh within [0, S*f)
+          if (n >= p.N) break;
+          float a[32];
+          ld_chunk(trow + c * 32, a);
+          const int s = n / p.f;
+          const int jj = n - s * p.f;
+          const int gcol = s * 2 * p.f + jj;
+          float dg[32], du[32], hw[32];
+          if (row_ok) {
+            const bf16* gsrc = p.gu + grow * p.ldgu + gcol;
+            const bf16* usrc = gsrc + p.f;
+            const bf16* hsrc = p.h + grow * p.ldh + n;
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                pk[e] = pack_bf16(__uint_as_float(r[v * 8 + 2 * e]) + bf16_lo(o[e]),
-                                  __uint_as_float(r[v * 8 + 2 * e + 1]) + bf16_hi(o[e]));
-              store16(dst + v * 8, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+            for (int vv = 0; vv < 4; ++vv) {
+              const uint4 G4 = *reinterpret_cast<const uint4*>(gsrc + vv * 8);
+              const uint4 U4 = *reinterpret_cast<const uint4*>(usrc + vv * 8);
+              const uint4 H4 = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
+              const uint32_t Gw[4] = {G4.x, G4.y, G4.z, G4.w};
+              const uint32_t Uw[4] = {U4.x, U4.y, U4.z, U4.w};
+              const uint32_t Hw[4] = {H4.x, H4.y, H4.z, H4.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int i = vv * 8 + e;
+                const float gg = (e & 1) ? bf16_hi(Gw[e >> 1]) : bf16_lo(Gw[e >> 1]);
+                const float uu = (e & 1) ? bf16_hi(Uw[e >> 1]) : bf16_lo(Uw[e >> 1]);
+                const float hh = (e & 1) ? bf16_hi(Hw[e >> 1]) : bf16_lo(Hw[e >> 1]);
+                dot = fmaf(a[i], hh, dot);
+                const float dh = w * a[i];
+                const float sg = sigmoidf_(gg);
+                dg[i] = dh * uu * sg * (1.0f + gg * (1.0f - sg));
+                du[i] = dh * gg * sg;
+                hw[i] = w * hh;
+              }
             }
           } else {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                pk[e] = pack_bf16(__uint_as_float(r[v * 8 + 2 * e]),
-                                  __uint_as_float(r[v * 8 + 2 * e + 1]));
-              store16(dst + v * 8, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+            for (int i = 0; i < 32; ++i) { dg[i] = 0.0f; du[i] = 0.0f; hw[i] = 0.0f; }
+          }
+          if (use_tma) {
+            stage_begin();
+            stage_bf16(stg, lane, dg);
+            stage_bf16(stg + 2048, lane, du);
+            if (p.aux) stage_bf16(stg + 4096, lane, hw);
+            stage_end();
+            if (lane == 0) {
+              tma_store_2d(sm.c0, stg_s, gcol, row0);
+              tma_store_2d(sm.c0, stg_s + 2048, gcol + p.f, row0);
+              if (p.aux) tma_store_2d(sm.c1, stg_s + 4096, n, row0);
+              bulk_commit();
             }
-          }
-        } else {
-          float* dst = reinterpret_cast<float*>(p.C) + off;
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            store16(dst + v * 4, make_uint4(r[v * 4], r[v * 4 + 1], r[v * 4 + 2], r[v * 4 + 3]));
-        }
-      }
-    } else if (p.epi == EPI_SWIGLU) {
-      // TMEM columns [0, BN/2) hold the gate, [BN/2, BN) the up projection.
-      const int out_batch = (p.b_batch_mode == BATCH_FROM_N) ? ti.batch : 0;
-#pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t rg[32], ru[32];
-        tmem_ld_32x32b_x32(trow + c * 32, rg);
-        tmem_ld_32x32b_x32(trow + BN / 2 + c * 32, ru);
-        tmem_ld_wait();
-        if (!row_ok) continue;
-        const int j = ti.nb0 + c * 32;
-        bf16* hdst = p.h + grow * p.ldh + static_cast<long long>(out_batch) * p.f + j;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = v * 8 + 2 * e;
-            const float g0 = __uint_as_float(rg[i0]), g1 = __uint_as_float(rg[i0 + 1]);
-            const float u0 = __uint_as_float(ru[i0]), u1 = __uint_as_float(ru[i0 + 1]);
-            pk[e] = pack_bf16(g0 * sigmoidf_(g0) * u0, g1 * sigmoidf_(g1) * u1);
-          }
-          store16(hdst + v * 8, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-        }
-        if (p.gu) {
-          bf16* gdst = p.gu + grow * p.ldgu + static_cast<long long>(out_batch) * 2 * p.f + j;
-          bf16* udst = gdst + p.f;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t pg[4], pu[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i0 = v * 8 + 2 * e;
-              pg[e] = pack_bf16(__uint_as_float(rg[i0]), __uint_as_float(rg[i0 + 1]));
-              pu[e] = pack_bf16(__uint_as_float(ru[i0]), __uint_as_float(ru[i0 + 1]));
-            }
-            store16(gdst + v * 8, make_uint4(pg[0], pg[1], pg[2], pg[3]));
-            store16(udst + v * 8, make_uint4(pu[0], pu[1], pu[2], pu[3]));
+            pending = true;
+          } else if (row_ok) {
+            bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + gcol;
+            store_bf16_row(dgdst, dg);
+            store_bf16_row(dgdst + p.f, du);
+            if (p.aux) store_bf16_row(p.aux + grow * p.ldaux + n, hw);
           }
         }
+        if (row_ok && p.dw_part) p.dw_part[grow * p.dw_nparts + ti.n_blk] = dot;
       }
-    } else if (p.epi == EPI_ROWSCALE) {
-      const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int n = ti.nb0 + c * 32;
-        if (n >= p.N) break;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(trow + c * 32, r);
-        tmem_ld_wait();
-        if (!row_ok) continue;
-        bf16* dst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + n;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            pk[e] = pack_bf16(w * __uint_as_float(r[v * 8 + 2 * e]),
-                              w * __uint_as_float(r[v * 8 + 2 * e + 1]));
-          store16(dst + v * 8, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-        }
-      }
-    } else {  // EPI_SWIGLU_BWD
-      const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
-      float dot = 0.0f;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int n = ti.nb0 + c * 32;  // column of dh within [0, S*f)
-        if (n >= p.N) break;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(trow + c * 32, r);
-        tmem_ld_wait();
-        if (!row_ok) continue;
-        const int s = n / p.f;
-        const int jj = n - s * p.f;
-        const bf16* gsrc = p.gu + grow * p.ldgu + static_cast<long long>(s) * 2 * p.f + jj;
-        const bf16* usrc = gsrc + p.f;
-        const bf16* hsrc = p.h + grow * p.ldh + n;
-        bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + static_cast<long long>(s) * 2 * p.f + jj;
-        bf16* dudst = dgdst + p.f;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint4 G4 = *reinterpret_cast<const uint4*>(gsrc + v * 8);
-          const uint4 U4 = *reinterpret_cast<const uint4*>(usrc + v * 8);
-          const uint4 H4 = *reinterpret_cast<const uint4*>(hsrc + v * 8);
-          const uint32_t Gw[4] = {G4.x, G4.y, G4.z, G4.w};
-          const uint32_t Uw[4] = {U4.x, U4.y, U4.z, U4.w};
-          const uint32_t Hw[4] = {H4.x, H4.y, H4.z, H4.w};
-          uint32_t pdg[4], pdu[4], phw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float dgv[2], duv[2], hwv[2];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const float a = __uint_as_float(r[v * 8 + 2 * e + hh]);
-              const float g = hh ? bf16_hi(Gw[e]) : bf16_lo(Gw[e]);
-              const float u = hh ? bf16_hi(Uw[e]) : bf16_lo(Uw[e]);
-              const float hv = hh ? bf16_hi(Hw[e]) : bf16_lo(Hw[e]);
-              dot = fmaf(a, hv, dot);
-              const float dh = w * a;
-              const float sg = sigmoidf_(g);
-              const float silu = g * sg;
-              dgv[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
-              duv[hh] = dh * silu;
-              hwv[hh] = w * hv;
-            }
-            pdg[e] = pack_bf16(dgv[0], dgv[1]);
-            pdu[e] = pack_bf16(duv[0], duv[1]);
-            phw[e] = pack_bf16(hwv[0], hwv[1]);
-          }
-          store16(dgdst + v * 8, make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]));
-          store16(dudst + v * 8, make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]));
-          if (p.aux)
-            store16(p.aux + grow * p.ldaux + n + v * 8, make_uint4(phw[0], phw[1], phw[2], phw[3]));
-        }
-      }
-      if (row_ok && p.dw_part) p.dw_part[grow * p.dw_nparts + ti.n_blk] = dot;
     }
     tc_fence_before();
     mbar_arrive(&tempty[buf]);
   }
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
 }
 
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
-                   const __grid_constant__ CUtensorMap mapB, const Params p) {
+                   const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapC0,
+                   const __grid_constant__ CUtensorMap mapC1, const Params p) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* staging = smem + C::STAGES * C::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + 4 * STAGING_PER_WARP);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -568,7 +661,8 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     mma_loop<BN>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
   } else {
-    epilogue_loop<BN>(p, tfull, tempty, tmem_base, abort_flag);
+    const StoreMaps sm{&mapC0, &mapC1, p.c0_rank3};
+    epilogue_loop<BN>(p, sm, staging, tfull, tempty, tmem_base, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -608,6 +702,25 @@ bool make_map(CUtensorMap* map, const MatView& v, int box_rows, bool force3d) {
                         const_cast<void*>(v.ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Tensor map of an output tensor [d2][d1][d0] (d0 contiguous) for 32x32-element
+// TMA stores: bf16 rows of 64 bytes with 64-byte swizzle, fp32 rows of 128 bytes
+// with 128-byte swizzle (the layouts stage_bf16 / stage_f32 write).
+bool make_store_map(CUtensorMap* map, void* ptr, bool f32, bool rank3, long long d0, long long d1,
+                    long long d2, long long ld, long long batch_stride) {
+  const long long es = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1),
+                        static_cast<cuuint64_t>(d2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * es),
+                           static_cast<cuuint64_t>(batch_stride * es)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        rank3 ? 3 : 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -666,9 +779,40 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   if (upper <= 0) return MOE_OK;
 
   if (!get_encoder()) return MOE_ERR_CUDA;
-  CUtensorMap mapA, mapB;
+  CUtensorMap mapA, mapB, mapC0, mapC1;
+  memset(&mapC0, 0, sizeof(mapC0));
+  memset(&mapC1, 0, sizeof(mapC1));
   if (!make_map(&mapA, L.A, L.a_mn ? 64 : BM, false)) return MOE_ERR_ARG;
   if (!make_map(&mapB, L.B, L.b_mn ? 64 : BN, b3)) return MOE_ERR_ARG;
+  // output (store) maps
+  const long long rows_out = (L.sched == SCHED_GROUPED_M) ? L.R_cap : L.M;
+  bool ok = true;
+  p.c0_rank3 = 0;
+  if (L.epi == EPI_STORE) {
+    if (!L.accumulate) {
+      const bool f32 = !L.c_bf16;
+      if (L.sched == SCHED_GROUPED_K) {
+        p.c0_rank3 = 1;
+        ok = make_store_map(&mapC0, L.C, f32, true, L.N, L.M, L.G, L.ldc, L.c_batch_stride);
+      } else if (L.c_batch_n > 0) {
+        p.c0_rank3 = 1;
+        ok = make_store_map(&mapC0, L.C, f32, true, L.c_batch_n, L.M, L.N / L.c_batch_n, L.ldc,
+                            L.c_batch_stride);
+      } else {
+        ok = make_store_map(&mapC0, L.C, f32, false, L.N, rows_out, 1, L.ldc, 0);
+      }
+    }
+  } else if (L.epi == EPI_SWIGLU) {
+    ok = make_store_map(&mapC0, L.h, false, false, L.ldh, rows_out, 1, L.ldh, 0);
+    if (ok && L.gu) ok = make_store_map(&mapC1, L.gu, false, false, L.ldgu, rows_out, 1, L.ldgu, 0);
+  } else if (L.epi == EPI_ROWSCALE) {
+    ok = make_store_map(&mapC0, L.C, false, false, L.N, rows_out, 1, L.ldc, 0);
+  } else {  // EPI_SWIGLU_BWD
+    ok = make_store_map(&mapC0, L.C, false, false, L.ldc, rows_out, 1, L.ldc, 0);
+    if (ok && L.aux)
+      ok = make_store_map(&mapC1, L.aux, false, false, L.ldaux, rows_out, 1, L.ldaux, 0);
+  }
+  if (!ok) return MOE_ERR_ARG;
 
   static bool attr_set[64] = {};
   int dev = 0;
@@ -686,7 +830,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
   {
     LaunchTimer lt(L.name, stream);
-    gemm_tc_kernel<BN><<<grid, 192, C::SMEM_BYTES, stream>>>(mapA, mapB, p);
+    gemm_tc_kernel<BN><<<grid, 192, C::SMEM_BYTES, stream>>>(mapA, mapB, mapC0, mapC1, p);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -39,7 +39,7 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 }
 
 template <int NPL>
-__global__ void __launch_bounds__(256) topk_sigmoid_kernel(const float* __restrict__ L,
+__global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __restrict__ L,
                                                            const float* __restrict__ bias, int T,
                                                            int E, int k, int* __restrict__ idx,
                                                            float* __restrict__ w_out,
