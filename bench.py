@@ -37,7 +37,7 @@ EXPERT_GEMMS = ("expert_gemm1_swiglu", "expert_gemm2_rowscale", "expert_dgrad2_s
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=4)
@@ -45,7 +45,23 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling case: override T (the JSON line then names that case)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling case: override E (the JSON line then names that case)")
     return ap.parse_args()
+
+
+def workload(args):
+    import dataclasses
+
+    from sparse_moe_layer_topk_gb300 import inputs as I
+    cfg = I.CONFIGS[args.config]
+    if args.tokens or args.experts:
+        T = args.tokens or cfg.T
+        E = args.experts or cfg.E
+        cfg = dataclasses.replace(cfg, T=T, E=E, name=f"profile_case_T{T}_E{E}_top{cfg.k}")
+    return cfg
 
 
 def dist_env():
@@ -160,7 +176,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -211,7 +227,7 @@ def oracle_sample_time(inp_cpu, n_tokens):
 def run_reference(args):
     world, rank, _ = dist_env()
     from sparse_moe_layer_topk_gb300 import inputs as I
-    cfg = I.CONFIGS[args.config]
+    cfg = workload(args)
     line = {"impl": "reference", "metric": METRIC, "unit": "tokens/s", "higher_is_better": True}
     if rank != 0:
         return
@@ -258,7 +274,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     M.load()
-    cfg = I.CONFIGS[args.config]
+    cfg = workload(args)
     T = cfg.T
     inp = I.make_layer_inputs(cfg)
     wdt = M.MOE_DTYPE_F32 if args.wgrad == "f32" else M.MOE_DTYPE_BF16

@@ -210,7 +210,8 @@ int moe_unpermute_combine_bwd(const uint16_t* dy_lat, const int32_t* token_of, i
  *   dW2[e]    = sum_r (row_w[r] h[r])^T dy_perm[r]                  ([E][f][l])
  *   dW13[e]   = sum_r z_perm[r]^T [dg|du][r]                         ([E][l][2f])
  * dW13/dW2 are fp32 or bf16 per wgrad_dtype; an expert with no rows gets exact
- * zeros. gu_save from the forward is required. Workspace:
+ * zeros. gu_save from the forward is required; h is recomputed from it in fp32
+ * (silu(g) * u), so `h` is not read and may be NULL. Workspace:
  * moe_workspace_size(MOE_OP_GROUPED_SWIGLU_BWD, 0, 0, l, E, 0, f, 0) with T*k = R
  * passed as T (k = 1). */
 int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, const uint16_t* W13,
@@ -222,7 +223,8 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
 
 /* Backward of moe_shared_swiglu for dy = d loss / d y_sh ([T][l]):
  *   dz_sh = sum_s [dg_s|du_s] @ W13_sh[s]^T (bf16 [T][l]); dW13_sh [S][l][2f];
- *   dW2_sh [S][f][l] (fp32 or bf16). gu_save and h from the forward are required.
+ *   dW2_sh [S][f][l] (fp32 or bf16). gu_save from the forward is required; `h`
+ *   (the forward's [T][S*f] SwiGLU output) is the A operand of the dW2_sh product.
  * Workspace: moe_workspace_size(MOE_OP_SHARED_SWIGLU_BWD, T, 0, 0, 0, 0, f, S). */
 int moe_shared_swiglu_bwd(const uint16_t* dy, const uint16_t* z, const uint16_t* W13_sh,
                           const uint16_t* W2_sh, const uint16_t* gu_save, const uint16_t* h,

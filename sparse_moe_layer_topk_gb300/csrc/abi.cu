@@ -389,14 +389,14 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
                            int E, int R, int l, int f, uint16_t* dz_perm, float* d_row_w,
                            void* dW13, void* dW2, int wgrad_dtype, void* ws, size_t ws_bytes,
                            void* stream) {
-  MOE_REQUIRE(dy_perm && z_perm && W13 && W2 && h && offsets && tile_sched && dz_perm && d_row_w &&
+  MOE_REQUIRE(dy_perm && z_perm && W13 && W2 && offsets && tile_sched && dz_perm && d_row_w &&
                   dW13 && dW2,
               MOE_ERR_ARG);
   MOE_REQUIRE(gu_save != nullptr, MOE_ERR_UNSUPPORTED);
   MOE_REQUIRE(E > 0 && R >= 0 && l > 0 && f > 0, MOE_ERR_ARG);
   MOE_REQUIRE(wgrad_dtype == MOE_DTYPE_F32 || wgrad_dtype == MOE_DTYPE_BF16, MOE_ERR_ARG);
   MOE_REQUIRE(l % 64 == 0 && f % 64 == 0, MOE_ERR_ALIGN);
-  MOE_REQUIRE(al16(dy_perm) && al16(z_perm) && al16(W13) && al16(W2) && al16(gu_save) && al16(h) &&
+  MOE_REQUIRE(al16(dy_perm) && al16(z_perm) && al16(W13) && al16(W2) && al16(gu_save) &&
                   al16(dz_perm) && al16(dW13) && al16(dW2),
               MOE_ERR_ALIGN);
   MOE_REQUIRE(ws != nullptr && ws_bytes >= grouped_bwd_ws(R, f), MOE_ERR_WORKSPACE);
@@ -433,8 +433,6 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
   D2.ldc = 2ll * f;
   D2.gu = const_cast<uint16_t*>(gu_save);
   D2.ldgu = 2ll * f;
-  D2.h = const_cast<uint16_t*>(h);
-  D2.ldh = f;
   D2.row_w = row_w;
   D2.aux = hw;
   D2.ldaux = f;

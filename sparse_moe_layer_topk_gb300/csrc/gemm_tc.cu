@@ -274,14 +274,13 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
         if (valid < BK) {
           // Rows past this expert's segment belong to the next expert: zero them
           // in every 64-wide chunk of A and B (rows are whole 128-byte lines).
-          const int nchunks = 2 + BN / 64;
-          const int per_chunk = (BK - valid) * 8;
+          const int n16 = (BK - valid) * 8;  // 16-byte pieces per chunk
           const uint4 zero = make_uint4(0, 0, 0, 0);
-          for (int i = lane; i < per_chunk * nchunks; i += 32) {
-            const int c = i / per_chunk;
-            const int rem = i - c * per_chunk;
-            const int row = valid + (rem >> 3);
-            *reinterpret_cast<uint4*>(sA + c * CHUNK_BYTES + row * 128 + (rem & 7) * 16) = zero;
+#pragma unroll
+          for (int c = 0; c < 2 + BN / 64; ++c) {
+            uint8_t* base = sA + c * CHUNK_BYTES + valid * 128;
+            for (int i = lane; i < n16; i += 32)
+              *reinterpret_cast<uint4*>(base + (i >> 3) * 128 + (i & 7) * 16) = zero;
           }
           fence_proxy_async_smem();
         }
@@ -542,10 +541,28 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
       } else {  // EPI_SWIGLU_BWD
         const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
         float dot = 0.0f;
+        // g and u of the next chunk are loaded one chunk ahead to hide their
+        // latency; h = silu(g) * u is recomputed from them (fp32) instead of
+        // being read back.
+        uint4 Gn[4], Un[4];
+        auto load_in = [&](int n, uint4* G, uint4* U) {
+          const int s = n / p.f;
+          const bf16* gsrc = p.gu + grow * p.ldgu + s * 2 * p.f + (n - s * p.f);
+#pragma unroll
+          for (int vv = 0; vv < 4; ++vv) {
+            G[vv] = *reinterpret_cast<const uint4*>(gsrc + vv * 8);
+            U[vv] = *reinterpret_cast<const uint4*>(gsrc + p.f + vv * 8);
+          }
+        };
+        if (row_ok && ti.nb0 < p.N) load_in(ti.nb0, Gn, Un);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           const int n = ti.nb0 + c * 32;  // column of dh within [0, S*f)
           if (n >= p.N) break;
+          uint4 Gc[4], Uc[4];
+#pragma unroll
+          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; }
+          if (row_ok && c + 1 < BN / 32 && n + 32 < p.N) load_in(n + 32, Gn, Un);
           float a[32];
           ld_chunk(trow + c * 32, a);
           const int s = n / p.f;
@@ -553,28 +570,23 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           const int gcol = s * 2 * p.f + jj;
           float dg[32], du[32], hw[32];
           if (row_ok) {
-            const bf16* gsrc = p.gu + grow * p.ldgu + gcol;
-            const bf16* usrc = gsrc + p.f;
-            const bf16* hsrc = p.h + grow * p.ldh + n;
 #pragma unroll
             for (int vv = 0; vv < 4; ++vv) {
-              const uint4 G4 = *reinterpret_cast<const uint4*>(gsrc + vv * 8);
-              const uint4 U4 = *reinterpret_cast<const uint4*>(usrc + vv * 8);
-              const uint4 H4 = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
+              const uint4 G4 = Gc[vv], U4 = Uc[vv];
               const uint32_t Gw[4] = {G4.x, G4.y, G4.z, G4.w};
               const uint32_t Uw[4] = {U4.x, U4.y, U4.z, U4.w};
-              const uint32_t Hw[4] = {H4.x, H4.y, H4.z, H4.w};
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const int i = vv * 8 + e;
                 const float gg = (e & 1) ? bf16_hi(Gw[e >> 1]) : bf16_lo(Gw[e >> 1]);
                 const float uu = (e & 1) ? bf16_hi(Uw[e >> 1]) : bf16_lo(Uw[e >> 1]);
-                const float hh = (e & 1) ? bf16_hi(Hw[e >> 1]) : bf16_lo(Hw[e >> 1]);
+                const float sg = sigmoidf_(gg);
+                const float silu = gg * sg;
+                const float hh = silu * uu;
                 dot = fmaf(a[i], hh, dot);
                 const float dh = w * a[i];
-                const float sg = sigmoidf_(gg);
                 dg[i] = dh * uu * sg * (1.0f + gg * (1.0f - sg));
-                du[i] = dh * gg * sg;
+                du[i] = dh * silu;
                 hw[i] = w * hh;
               }
             }
