@@ -210,8 +210,7 @@ int moe_unpermute_combine_bwd(const uint16_t* dy_lat, const int32_t* token_of, i
  *   dW2[e]    = sum_r (row_w[r] h[r])^T dy_perm[r]                  ([E][f][l])
  *   dW13[e]   = sum_r z_perm[r]^T [dg|du][r]                         ([E][l][2f])
  * dW13/dW2 are fp32 or bf16 per wgrad_dtype; an expert with no rows gets exact
- * zeros. gu_save from the forward is required; h is recomputed from it in fp32
- * (silu(g) * u), so `h` is not read and may be NULL. Workspace:
+ * zeros. gu_save and h from the forward are required. Workspace:
  * moe_workspace_size(MOE_OP_GROUPED_SWIGLU_BWD, 0, 0, l, E, 0, f, 0) with T*k = R
  * passed as T (k = 1). */
 int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, const uint16_t* W13,

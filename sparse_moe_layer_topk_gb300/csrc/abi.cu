@@ -112,7 +112,9 @@ struct WsCarver {
 };
 
 size_t grouped_bwd_ws(long long R, int f) {
-  const int nparts = (f + 127) / 128;  // upper bound of n tiles of the SwiGLU-backward GEMM
+  // upper bound of the routing-weight partials per row: 2 epilogue warp groups
+  // x n tiles (tiles are at least 128 wide)
+  const int nparts = 2 * ((f + 127) / 128);
   return up256(static_cast<size_t>(R) * 2 * f * 2) + up256(static_cast<size_t>(R) * f * 2) +
          up256(static_cast<size_t>(R) * nparts * 4);
 }
@@ -389,14 +391,14 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
                            int E, int R, int l, int f, uint16_t* dz_perm, float* d_row_w,
                            void* dW13, void* dW2, int wgrad_dtype, void* ws, size_t ws_bytes,
                            void* stream) {
-  MOE_REQUIRE(dy_perm && z_perm && W13 && W2 && offsets && tile_sched && dz_perm && d_row_w &&
+  MOE_REQUIRE(dy_perm && z_perm && W13 && W2 && h && offsets && tile_sched && dz_perm && d_row_w &&
                   dW13 && dW2,
               MOE_ERR_ARG);
   MOE_REQUIRE(gu_save != nullptr, MOE_ERR_UNSUPPORTED);
   MOE_REQUIRE(E > 0 && R >= 0 && l > 0 && f > 0, MOE_ERR_ARG);
   MOE_REQUIRE(wgrad_dtype == MOE_DTYPE_F32 || wgrad_dtype == MOE_DTYPE_BF16, MOE_ERR_ARG);
   MOE_REQUIRE(l % 64 == 0 && f % 64 == 0, MOE_ERR_ALIGN);
-  MOE_REQUIRE(al16(dy_perm) && al16(z_perm) && al16(W13) && al16(W2) && al16(gu_save) &&
+  MOE_REQUIRE(al16(dy_perm) && al16(z_perm) && al16(W13) && al16(W2) && al16(gu_save) && al16(h) &&
                   al16(dz_perm) && al16(dW13) && al16(dW2),
               MOE_ERR_ALIGN);
   MOE_REQUIRE(ws != nullptr && ws_bytes >= grouped_bwd_ws(R, f), MOE_ERR_WORKSPACE);
@@ -410,7 +412,8 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
   WsCarver wc{reinterpret_cast<char*>(ws), ws_bytes};
   uint16_t* dgu = reinterpret_cast<uint16_t*>(wc.take(static_cast<size_t>(R) * 2 * f * 2));
   uint16_t* hw = reinterpret_cast<uint16_t*>(wc.take(static_cast<size_t>(R) * f * 2));
-  float* dw_part = reinterpret_cast<float*>(wc.take(static_cast<size_t>(R) * ((f + 127) / 128) * 4));
+  float* dw_part =
+      reinterpret_cast<float*>(wc.take(static_cast<size_t>(R) * 2 * ((f + 127) / 128) * 4));
   MOE_REQUIRE(wc.ok, MOE_ERR_WORKSPACE);
   // 1. dgrad through W2 with the SwiGLU backward and routing-weight dots fused
   GemmLaunch D2;
@@ -433,11 +436,13 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
   D2.ldc = 2ll * f;
   D2.gu = const_cast<uint16_t*>(gu_save);
   D2.ldgu = 2ll * f;
+  D2.h = const_cast<uint16_t*>(h);
+  D2.ldh = f;
   D2.row_w = row_w;
   D2.aux = hw;
   D2.ldaux = f;
   D2.dw_part = dw_part;
-  D2.dw_nparts = (f + D2.BN - 1) / D2.BN;
+  D2.dw_nparts = (gemm_epilogue_warps(D2) / 4) * ((f + D2.BN - 1) / D2.BN);
   if (R > 0) MOE_CHECK(gemm_launch(D2, st));
   MOE_CHECK(cuda_status(launch_dw_reduce(dw_part, D2.dw_nparts, R, d_row_w, st)));
   // 2. dW2[e] = (row_w h)^T dy_perm over the expert's rows (ragged K)

@@ -240,6 +240,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+// Epilogue sigmoid: CUDA's fast exp and division intrinsics (a few ulp; the
+// router's weights use the accurate expf and an IEEE division instead).
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 }  // namespace moe

@@ -79,6 +79,11 @@ struct GemmLaunch {
 // Returns MOE_OK or an MOE_ERR_* code (argument checks, launch errors).
 int gemm_launch(const GemmLaunch& L, cudaStream_t stream);
 
+// Number of epilogue warps gemm_launch uses for L (4 or 8). With 8, two warps
+// share each accumulator row and EPI_SWIGLU_BWD writes two routing-weight
+// partials per row and n tile (dw_nparts = 2 * n tiles).
+int gemm_epilogue_warps(const GemmLaunch& L);
+
 int num_sms();
 void record_cuda_error(cudaError_t e);
 

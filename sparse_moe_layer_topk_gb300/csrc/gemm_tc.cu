@@ -37,13 +37,16 @@ constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int CHUNK_BYTES = 64 * 128;  // one 64-row x 128-byte swizzled block
 
-template <int BN>
+// BN: tile width (UMMA N); EW: epilogue warps (4, or 8 for heavy epilogues:
+// two warps per TMEM lane quadrant, splitting the tile's column chunks).
+template <int BN, int EW>
 struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int STAGES = (BN == 256) ? (EW == 8 ? 3 : 4) : (EW == 8 ? 5 : 6);
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * 6144 + 1024 + 256;
+  static constexpr int THREADS = 64 + 32 * EW;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * 6144 + 1024 + 256;
 };
 
 struct Params {
@@ -156,11 +159,11 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* err_f
 
 // ------------------------------------------------------------------ producer
 
-template <int BN>
+template <int BN, int EW>
 __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CUtensorMap* mapB,
                               uint8_t* smem, uint64_t* full, uint64_t* empty,
                               volatile int* abort_flag) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EW>;
   int stage = 0;
   uint32_t phase = 0;
   long long issued = 0;
@@ -236,11 +239,11 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
 
 // ------------------------------------------------------------------ MMA
 
-template <int BN>
+template <int BN, int EW>
 __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                          uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
                          volatile int* abort_flag) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EW>;
   const uint32_t lane = lane_id();
   const uint32_t idesc = make_idesc_bf16(BM, BN, p.a_mn, p.b_mn);
   const uint32_t a_lbo = p.a_mn ? CHUNK_BYTES : 16, b_lbo = p.b_mn ? CHUNK_BYTES : 16;
@@ -383,12 +386,14 @@ struct StoreMaps {
   int c0_rank3;
 };
 
-template <int BN>
+template <int BN, int EW>
 __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* staging,
                               uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base,
                               volatile int* abort_flag) {
+  constexpr int NG = EW / 4;  // warps per TMEM lane quadrant; they split the column chunks
   const int warp = threadIdx.x >> 5;
   const int q = warp & 3;  // tensor-memory lane quadrant this warp may read
+  const int grp = (warp - 2) / 4;
   const uint32_t lane = lane_id();
   const int r_loc = q * 32 + static_cast<int>(lane);
   uint8_t* stg = staging + (warp - 2) * STAGING_PER_WARP;
@@ -428,7 +433,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
     if (blk_rows > 0) {
       if (p.epi == EPI_STORE) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = grp; c < BN / 32; c += NG) {
           const int n = ti.nb0 + c * 32;
           if (n >= p.N) break;  // warp-uniform N tail
           float v[32];
@@ -481,7 +486,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
         // TMEM columns [0, BN/2) hold the gate, [BN/2, BN) the up projection.
         const int out_batch = (p.b_batch_mode == BATCH_FROM_N) ? ti.batch : 0;
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int c = grp; c < BN / 64; c += NG) {
           float g[32], u[32], hv[32];
           ld_chunk(trow + c * 32, g);
           ld_chunk(trow + BN / 2 + c * 32, u);
@@ -518,7 +523,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
       } else if (p.epi == EPI_ROWSCALE) {
         const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = grp; c < BN / 32; c += NG) {
           const int n = ti.nb0 + c * 32;
           if (n >= p.N) break;
           float v[32];
@@ -541,11 +546,11 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
       } else {  // EPI_SWIGLU_BWD
         const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
         float dot = 0.0f;
-        // g and u of the next chunk are loaded one chunk ahead to hide their
-        // latency; h = silu(g) * u is recomputed from them (fp32) instead of
-        // being read back.
+        // g and u of the next chunk are loaded one chunk ahead, h of the current
+        // chunk at its start (it is needed last); results go to the staging
+        // blocks 8 columns at a time to keep the register footprint small.
         uint4 Gn[4], Un[4];
-        auto load_in = [&](int n, uint4* G, uint4* U) {
+        auto load_gu = [&](int n, uint4* G, uint4* U) {
           const int s = n / p.f;
           const bf16* gsrc = p.gu + grow * p.ldgu + s * 2 * p.f + (n - s * p.f);
 #pragma unroll
@@ -554,51 +559,72 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             U[vv] = *reinterpret_cast<const uint4*>(gsrc + p.f + vv * 8);
           }
         };
-        if (row_ok && ti.nb0 < p.N) load_in(ti.nb0, Gn, Un);
+        const uint4 z4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
+        if (row_ok && ti.nb0 + grp * 32 < p.N) load_gu(ti.nb0 + grp * 32, Gn, Un);
+        const int sw = (lane >> 1) & 3;  // 64-byte swizzle of this lane's staging row
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = grp; c < BN / 32; c += NG) {
           const int n = ti.nb0 + c * 32;  // column of dh within [0, S*f)
           if (n >= p.N) break;
-          uint4 Gc[4], Uc[4];
+          uint4 Gc[4], Uc[4], Hc[4];
 #pragma unroll
-          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; }
-          if (row_ok && c + 1 < BN / 32 && n + 32 < p.N) load_in(n + 32, Gn, Un);
+          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; Hc[vv] = z4; }
+          if (row_ok) {
+            const bf16* hsrc = p.h + grow * p.ldh + n;
+#pragma unroll
+            for (int vv = 0; vv < 4; ++vv) Hc[vv] = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
+            if (c + NG < BN / 32 && n + 32 * NG < p.N) load_gu(n + 32 * NG, Gn, Un);
+          }
           float a[32];
           ld_chunk(trow + c * 32, a);
           const int s = n / p.f;
           const int jj = n - s * p.f;
           const int gcol = s * 2 * p.f + jj;
-          float dg[32], du[32], hw[32];
-          if (row_ok) {
+          if (use_tma) stage_begin();
+          bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + gcol;
 #pragma unroll
-            for (int vv = 0; vv < 4; ++vv) {
-              const uint4 G4 = Gc[vv], U4 = Uc[vv];
-              const uint32_t Gw[4] = {G4.x, G4.y, G4.z, G4.w};
-              const uint32_t Uw[4] = {U4.x, U4.y, U4.z, U4.w};
+          for (int vv = 0; vv < 4; ++vv) {
+            const uint32_t Gw[4] = {Gc[vv].x, Gc[vv].y, Gc[vv].z, Gc[vv].w};
+            const uint32_t Uw[4] = {Uc[vv].x, Uc[vv].y, Uc[vv].z, Uc[vv].w};
+            const uint32_t Hw[4] = {Hc[vv].x, Hc[vv].y, Hc[vv].z, Hc[vv].w};
+            uint32_t pdg[4], pdu[4], phw[4];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int i = vv * 8 + e;
-                const float gg = (e & 1) ? bf16_hi(Gw[e >> 1]) : bf16_lo(Gw[e >> 1]);
-                const float uu = (e & 1) ? bf16_hi(Uw[e >> 1]) : bf16_lo(Uw[e >> 1]);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              float dgv[2], duv[2], hwv[2];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const float av = a[vv * 8 + 2 * e2 + hh];
+                const float gg = hh ? bf16_hi(Gw[e2]) : bf16_lo(Gw[e2]);
+                const float uu = hh ? bf16_hi(Uw[e2]) : bf16_lo(Uw[e2]);
+                const float hv = hh ? bf16_hi(Hw[e2]) : bf16_lo(Hw[e2]);
                 const float sg = sigmoidf_(gg);
-                const float silu = gg * sg;
-                const float hh = silu * uu;
-                dot = fmaf(a[i], hh, dot);
-                const float dh = w * a[i];
-                dg[i] = dh * uu * sg * (1.0f + gg * (1.0f - sg));
-                du[i] = dh * silu;
-                hw[i] = w * hh;
+                const float dh = w * av;
+                dgv[hh] = dh * uu * sg * (1.0f + gg * (1.0f - sg));
+                duv[hh] = dh * gg * sg;
+                dot = fmaf(av, hv, dot);
+                hwv[hh] = w * hv;
               }
+              pdg[e2] = pack_bf16(dgv[0], dgv[1]);
+              pdu[e2] = pack_bf16(duv[0], duv[1]);
+              phw[e2] = pack_bf16(hwv[0], hwv[1]);
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) { dg[i] = 0.0f; du[i] = 0.0f; hw[i] = 0.0f; }
+            const uint4 DG = make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]);
+            const uint4 DU = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
+            const uint4 HW = make_uint4(phw[0], phw[1], phw[2], phw[3]);
+            if (use_tma) {
+              const int off = lane * 64 + ((vv ^ sw) << 4);
+              *reinterpret_cast<uint4*>(stg + off) = DG;
+              *reinterpret_cast<uint4*>(stg + 2048 + off) = DU;
+              if (p.aux) *reinterpret_cast<uint4*>(stg + 4096 + off) = HW;
+            } else if (row_ok) {
+              store16(dgdst + vv * 8, DG);
+              store16(dgdst + p.f + vv * 8, DU);
+              if (p.aux) store16(p.aux + grow * p.ldaux + n + vv * 8, HW);
+            }
           }
           if (use_tma) {
-            stage_begin();
-            stage_bf16(stg, lane, dg);
-            stage_bf16(stg + 2048, lane, du);
-            if (p.aux) stage_bf16(stg + 4096, lane, hw);
             stage_end();
             if (lane == 0) {
               tma_store_2d(sm.c0, stg_s, gcol, row0);
@@ -607,14 +633,9 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
               bulk_commit();
             }
             pending = true;
-          } else if (row_ok) {
-            bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + gcol;
-            store_bf16_row(dgdst, dg);
-            store_bf16_row(dgdst + p.f, du);
-            if (p.aux) store_bf16_row(p.aux + grow * p.ldaux + n, hw);
           }
         }
-        if (row_ok && p.dw_part) p.dw_part[grow * p.dw_nparts + ti.n_blk] = dot;
+        if (row_ok && p.dw_part) p.dw_part[grow * p.dw_nparts + ti.n_blk * NG + grp] = dot;
       }
     }
     tc_fence_before();
@@ -624,18 +645,18 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   __syncwarp();
 }
 
-template <int BN>
-__global__ void __launch_bounds__(192, 1)
+template <int BN, int EW>
+__global__ void __launch_bounds__(64 + 32 * EW, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC0,
                    const __grid_constant__ CUtensorMap mapC1, const Params p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* staging = smem + C::STAGES * C::STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + 4 * STAGING_PER_WARP);
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + EW * STAGING_PER_WARP);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -651,7 +672,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 32 * EW);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -669,12 +690,12 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane_id() == 0) producer_loop<BN>(p, &mapA, &mapB, smem, full, empty, abort_flag);
+    if (lane_id() == 0) producer_loop<BN, EW>(p, &mapA, &mapB, smem, full, empty, abort_flag);
   } else if (warp == 1) {
-    mma_loop<BN>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
+    mma_loop<BN, EW>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
   } else {
     const StoreMaps sm{&mapC0, &mapC1, p.c0_rank3};
-    epilogue_loop<BN>(p, sm, staging, tfull, tempty, tmem_base, abort_flag);
+    epilogue_loop<BN, EW>(p, sm, staging, tfull, tempty, tmem_base, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -736,9 +757,9 @@ bool make_store_map(CUtensorMap* map, void* ptr, bool f32, bool rank3, long long
   return r == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, int EW>
 int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EW>;
   Params p{};
   p.sched = L.sched;
   p.M = L.M;
@@ -826,11 +847,11 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   }
   if (!ok) return MOE_ERR_ARG;
 
-  static bool attr_set[64] = {};
+  static bool attr_set[64] = {};  // one flag per device and template instance
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) {
@@ -842,7 +863,8 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
   {
     LaunchTimer lt(L.name, stream);
-    gemm_tc_kernel<BN><<<grid, 192, C::SMEM_BYTES, stream>>>(mapA, mapB, mapC0, mapC1, p);
+    gemm_tc_kernel<BN, EW><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mapA, mapB, mapC0, mapC1,
+                                                                          p);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -854,9 +876,18 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
 
 }  // namespace
 
+int gemm_epilogue_warps(const GemmLaunch& L) {
+  // The fused SwiGLU epilogues do enough arithmetic and loads per element
+  // that one warp per TMEM lane quadrant cannot hide their latency: they get
+  // 8 warps (and one pipeline stage less). Plain stores keep 4 warps and the
+  // deeper pipeline.
+  return (L.epi == EPI_SWIGLU || L.epi == EPI_SWIGLU_BWD) ? 8 : 4;
+}
+
 int gemm_launch(const GemmLaunch& L, cudaStream_t stream) {
-  if (L.BN == 256) return launch_bn<256>(L, stream);
-  if (L.BN == 128) return launch_bn<128>(L, stream);
+  const int ew = gemm_epilogue_warps(L);
+  if (L.BN == 256) return ew == 8 ? launch_bn<256, 8>(L, stream) : launch_bn<256, 4>(L, stream);
+  if (L.BN == 128) return ew == 8 ? launch_bn<128, 8>(L, stream) : launch_bn<128, 4>(L, stream);
   return MOE_ERR_UNSUPPORTED;
 }
 
