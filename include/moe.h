@@ -224,7 +224,8 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
  *   dz_sh = sum_s [dg_s|du_s] @ W13_sh[s]^T (bf16 [T][l]); dW13_sh [S][l][2f];
  *   dW2_sh [S][f][l] (fp32 or bf16). gu_save from the forward is required; `h`
  *   (the forward's [T][S*f] SwiGLU output) is the A operand of the dW2_sh product.
- * Workspace: moe_workspace_size(MOE_OP_SHARED_SWIGLU_BWD, T, 0, 0, 0, 0, f, S). */
+ * Workspace: moe_workspace_size(MOE_OP_SHARED_SWIGLU_BWD, T, 0, l, 0, 0, f, S) (the gate/up
+ * gradients plus, at large T, fp32 partials of the K-split weight gradients). */
 int moe_shared_swiglu_bwd(const uint16_t* dy, const uint16_t* z, const uint16_t* W13_sh,
                           const uint16_t* W2_sh, const uint16_t* gu_save, const uint16_t* h,
                           int T, int l, int f, int S, uint16_t* dz_sh, void* dW13_sh,

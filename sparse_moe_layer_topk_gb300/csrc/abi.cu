@@ -1,6 +1,7 @@
 // C-ABI entry points of libmoe: host-side argument checks, workspace carving
 // and the launch sequence of each step. Every entry point enqueues work on
 // the caller's stream and returns; none allocates, frees or synchronises.
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 
@@ -69,7 +70,25 @@ MatView view(const void* p, long long rows, long long cols, long long ld, long l
   return v;
 }
 
-inline int pick_bn(int N) { return (N % 256 == 0) ? 256 : 128; }
+// Tile width: 256 unless N is narrow or a 256-wide tail would waste more than a quarter.
+inline int pick_bn(int N) { return (N % 256 == 0 || (N > 512 && N % 256 >= 128)) ? 256 : 128; }
+
+// K slices for a dense wgrad with few output tiles (K = tokens, long): enough
+// slices to give ~128 tiles, at most 4, each slice at least 1024 rows of K.
+inline int wgrad_splitk(int M, int N, int K) {
+  const int bn = pick_bn(N);
+  const int tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+  int s = 1;
+  while (s < 4 && tiles * s * 2 <= 128 && K / (s * 2) >= 1024) s *= 2;
+  return s;
+}
+
+size_t shared_bwd_ws(int T, int l, int f, int S_) {
+  const long long Sf = static_cast<long long>(S_) * f;
+  const size_t split = std::max(gemm_splitk_ws_bytes(Sf, l, wgrad_splitk(static_cast<int>(Sf), l, T)),
+                                gemm_splitk_ws_bytes(l, 2 * Sf, wgrad_splitk(l, static_cast<int>(2 * Sf), T)));
+  return up256(static_cast<size_t>(T) * Sf * 2 * 2) + up256(split);
+}
 
 // C[M][N] (bf16 or fp32) = A[M][K] @ B, B given as [K][N] (b_mn) or [N][K].
 int dense_gemm(const char* name, const void* A, long long lda, int a_mn, const void* B,
@@ -147,7 +166,7 @@ size_t moe_workspace_size(int op, int T, int d, int l, int E, int k, int f, int 
     case MOE_OP_PERMUTE: return up256(static_cast<size_t>(permute_chunks(T)) * E * 4);
     case MOE_OP_GROUPED_SWIGLU_BWD:
       return grouped_bwd_ws(static_cast<long long>(T) * (k > 0 ? k : 1), f);
-    case MOE_OP_SHARED_SWIGLU_BWD: return up256(static_cast<size_t>(T) * S * 2 * f * 2);
+    case MOE_OP_SHARED_SWIGLU_BWD: return shared_bwd_ws(T, l, f, S);
     case MOE_OP_ROUTE_TOPK_BWD: return up256(static_cast<size_t>(T) * E * 2);
     default: return 0;
   }
@@ -518,9 +537,7 @@ int moe_shared_swiglu_bwd(const uint16_t* dy, const uint16_t* z, const uint16_t*
   MOE_REQUIRE(al16(dy) && al16(z) && al16(W13_sh) && al16(W2_sh) && al16(gu_save) && al16(h) &&
                   al16(dz_sh) && al16(dW13_sh) && al16(dW2_sh),
               MOE_ERR_ALIGN);
-  MOE_REQUIRE(ws != nullptr &&
-                  ws_bytes >= moe_workspace_size(MOE_OP_SHARED_SWIGLU_BWD, T, 0, l, 0, 0, f, S_),
-              MOE_ERR_WORKSPACE);
+  MOE_REQUIRE(ws != nullptr && ws_bytes >= shared_bwd_ws(T, l, f, S_), MOE_ERR_WORKSPACE);
   cudaStream_t st = S(stream);
   const int wbf16 = wgrad_dtype == MOE_DTYPE_BF16;
   const long long Sf = static_cast<long long>(S_) * f;
@@ -530,6 +547,8 @@ int moe_shared_swiglu_bwd(const uint16_t* dy, const uint16_t* z, const uint16_t*
     return cuda_status(cudaMemsetAsync(dW2_sh, 0, static_cast<size_t>(Sf) * l * es, st));
   }
   uint16_t* dgu = reinterpret_cast<uint16_t*>(ws);
+  float* split_ws = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) +
+                                             up256(static_cast<size_t>(T) * Sf * 2 * 2));
   // 1. dh = dy W2_sh^T (all shared experts at once), SwiGLU backward fused
   GemmLaunch D2;
   D2.name = "shared_dgrad2_swiglu_bwd";
@@ -550,8 +569,27 @@ int moe_shared_swiglu_bwd(const uint16_t* dy, const uint16_t* z, const uint16_t*
   D2.h = const_cast<uint16_t*>(h);
   D2.ldh = Sf;
   MOE_CHECK(gemm_launch(D2, st));
-  // 2. dW2_sh [S*f][l] = h^T dy
-  MOE_CHECK(dense_gemm("shared_wgrad2", h, Sf, 1, dy, l, 1, static_cast<int>(Sf), l, T, dW2_sh, l, wbf16, 0, st));
+  // 2. dW2_sh [S*f][l] = h^T dy (K = T split into slices when there are few tiles)
+  {
+    GemmLaunch W2s;
+    W2s.name = "shared_wgrad2";
+    W2s.BN = pick_bn(l);
+    W2s.sched = SCHED_DENSE;
+    W2s.M = static_cast<int>(Sf);
+    W2s.N = l;
+    W2s.K = T;
+    W2s.A = view(h, T, Sf, Sf);
+    W2s.a_mn = 1;
+    W2s.B = view(dy, T, l, l);
+    W2s.b_mn = 1;
+    W2s.epi = EPI_STORE;
+    W2s.C = dW2_sh;
+    W2s.ldc = l;
+    W2s.c_bf16 = wbf16;
+    W2s.splitk = wgrad_splitk(W2s.M, W2s.N, T);
+    W2s.splitk_ws = split_ws;
+    MOE_CHECK(gemm_launch(W2s, st));
+  }
   // 3. dz_sh = sum_s [dg_s|du_s] W13_sh[s]^T: one GEMM with K = S*2f, B batch from K
   GemmLaunch D1;
   D1.name = "shared_dgrad1";
@@ -588,6 +626,8 @@ int moe_shared_swiglu_bwd(const uint16_t* dy, const uint16_t* z, const uint16_t*
   W1g.c_batch_n = 2 * f;
   W1g.c_batch_stride = static_cast<long long>(l) * 2 * f;
   W1g.c_bf16 = wbf16;
+  W1g.splitk = wgrad_splitk(W1g.M, W1g.N, T);
+  W1g.splitk_ws = split_ws;
   return gemm_launch(W1g, st);
 }
 

@@ -74,7 +74,17 @@ struct GemmLaunch {
   float* dw_part = nullptr;
   int dw_nparts = 0;
   int* err_flag = nullptr;
+  // Split-K (dense EPI_STORE only): K is cut into `splitk` slices whose fp32
+  // partial products go to splitk_ws [splitk][M][N]; a reduce kernel then
+  // writes C. Deterministic (fixed summation order).
+  int splitk = 1;
+  float* splitk_ws = nullptr;
 };
+
+// Bytes of split workspace gemm_launch needs for M x N with `splitk` slices.
+inline size_t gemm_splitk_ws_bytes(long long M, long long N, int splitk) {
+  return splitk > 1 ? static_cast<size_t>(splitk) * M * N * 4 : 0;
+}
 
 // Returns MOE_OK or an MOE_ERR_* code (argument checks, launch errors).
 int gemm_launch(const GemmLaunch& L, cudaStream_t stream);

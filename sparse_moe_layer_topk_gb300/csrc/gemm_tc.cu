@@ -57,6 +57,7 @@ struct Params {
   int b_batch_mode, n_tiles_per_batch, k_per_batch;
   int swiglu_b, f;
   int mt, nt;         // m tiles (dense / grouped-K), n tiles
+  int splitk, kslice; // dense: K split into `splitk` slices of `kslice` (multiple of 64)
   int total_static;   // tile count when it does not depend on device data
   int epi;
   void* C;
@@ -133,7 +134,10 @@ __device__ __forceinline__ Tile decode(const Params& p, int t) {
     ti.krows = seg1 - seg0;
     ti.nk = (ti.krows + BK - 1) / BK;
   } else {
-    ti.g = 0;
+    // split-K: the slice index is the outer tile index and takes the role of g
+    const int per = p.mt * p.nt;
+    ti.g = t / per;
+    t -= ti.g * per;
     ti.n_blk = t / p.mt;
     const int m_blk = t - ti.n_blk * p.mt;
     ti.m0 = m_blk * BM;
@@ -145,9 +149,9 @@ __device__ __forceinline__ Tile decode(const Params& p, int t) {
       ti.batch = 0;
       ti.nb0 = ti.n_blk * bn_eff;
     }
-    ti.k0 = 0;
-    ti.krows = p.K;
-    ti.nk = (p.K + BK - 1) / BK;
+    ti.k0 = ti.g * p.kslice;
+    ti.krows = min(p.kslice, p.K - ti.k0);
+    ti.nk = (ti.krows + BK - 1) / BK;
   }
   return ti;
 }
@@ -444,8 +448,8 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
           int ncol = n, cb = 0;
-          if (p.sched == SCHED_GROUPED_K) {
-            cb = ti.g;
+          if (p.sched == SCHED_GROUPED_K || p.splitk > 1) {
+            cb = ti.g;  // expert (grouped-K) or K slice (split-K partials)
           } else if (p.c_batch_n > 0) {
             cb = n / p.c_batch_n;
             ncol = n - cb * p.c_batch_n;
@@ -782,7 +786,10 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   p.mt = (L.M + BM - 1) / BM;
   long long upper;
   if (L.sched == SCHED_DENSE) {
-    p.total_static = p.mt * p.nt;
+    p.splitk = L.splitk > 1 ? L.splitk : 1;
+    p.kslice = ((L.K + p.splitk - 1) / p.splitk + BK - 1) / BK * BK;
+    p.splitk = (L.K + p.kslice - 1) / p.kslice;
+    p.total_static = p.mt * p.nt * p.splitk;
     upper = p.total_static;
   } else if (L.sched == SCHED_GROUPED_K) {
     p.total_static = L.G * p.mt * p.nt;
@@ -827,6 +834,13 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
       if (L.sched == SCHED_GROUPED_K) {
         p.c0_rank3 = 1;
         ok = make_store_map(&mapC0, L.C, f32, true, L.N, L.M, L.G, L.ldc, L.c_batch_stride);
+      } else if (p.splitk > 1) {
+        // fp32 partial sums per K slice into the caller's split workspace [splitk][M][N]
+        if (!L.splitk_ws) return MOE_ERR_WORKSPACE;
+        p.c0_rank3 = 1;
+        p.c_bf16 = 0;
+        ok = make_store_map(&mapC0, L.splitk_ws, true, true, L.N, L.M, p.splitk, L.N,
+                            static_cast<long long>(L.M) * L.N);
       } else if (L.c_batch_n > 0) {
         p.c0_rank3 = 1;
         ok = make_store_map(&mapC0, L.C, f32, true, L.c_batch_n, L.M, L.N / L.c_batch_n, L.ldc,
@@ -876,6 +890,39 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
 
 }  // namespace
 
+// out (fp32 or bf16, layout of the GEMM's C) = sum over K slices of the fp32
+// partials ws[s][m][n]; four columns per thread, slices summed in order.
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splitk, int M, int N,
+                                     void* __restrict__ out, int out_bf16, long long ldc,
+                                     int c_batch_n, long long c_batch_stride) {
+  const long long n4 = static_cast<long long>(M) * (N / 4);
+  const long long MN = static_cast<long long>(M) * N;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long m = i / (N / 4);
+    const int n = static_cast<int>(i - m * (N / 4)) * 4;
+    float4 acc = *reinterpret_cast<const float4*>(ws + m * N + n);
+    for (int sl = 1; sl < splitk; ++sl) {
+      const float4 v = *reinterpret_cast<const float4*>(ws + sl * MN + m * N + n);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    int col = n;
+    long long base = 0;
+    if (c_batch_n > 0) {
+      const int cb = n / c_batch_n;
+      col = n - cb * c_batch_n;
+      base = cb * c_batch_stride;
+    }
+    const long long o = base + m * ldc + col;
+    if (out_bf16) {
+      uint2 pk = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+      *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(out) + o) = pk;
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + o) = acc;
+    }
+  }
+}
+
 int gemm_epilogue_warps(const GemmLaunch& L) {
   // The fused SwiGLU epilogues do enough arithmetic and loads per element
   // that one warp per TMEM lane quadrant cannot hide their latency: they get
@@ -886,9 +933,29 @@ int gemm_epilogue_warps(const GemmLaunch& L) {
 
 int gemm_launch(const GemmLaunch& L, cudaStream_t stream) {
   const int ew = gemm_epilogue_warps(L);
-  if (L.BN == 256) return ew == 8 ? launch_bn<256, 8>(L, stream) : launch_bn<256, 4>(L, stream);
-  if (L.BN == 128) return ew == 8 ? launch_bn<128, 8>(L, stream) : launch_bn<128, 4>(L, stream);
-  return MOE_ERR_UNSUPPORTED;
+  if (L.splitk > 1 && !(L.sched == SCHED_DENSE && L.epi == EPI_STORE && !L.accumulate))
+    return MOE_ERR_UNSUPPORTED;
+  int st;
+  if (L.BN == 256) st = ew == 8 ? launch_bn<256, 8>(L, stream) : launch_bn<256, 4>(L, stream);
+  else if (L.BN == 128) st = ew == 8 ? launch_bn<128, 8>(L, stream) : launch_bn<128, 4>(L, stream);
+  else return MOE_ERR_UNSUPPORTED;
+  if (st != MOE_OK || L.splitk <= 1) return st;
+  const int kslice = ((L.K + L.splitk - 1) / L.splitk + BK - 1) / BK * BK;
+  const int nslices = (L.K + kslice - 1) / kslice;
+  const long long n4 = static_cast<long long>(L.M) * (L.N / 4);
+  long long blocks = (n4 + 255) / 256;
+  if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
+  {
+    LaunchTimer lt("splitk_reduce", stream);
+    splitk_reduce_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        L.splitk_ws, nslices, L.M, L.N, L.C, L.c_bf16, L.ldc, L.c_batch_n, L.c_batch_stride);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 }  // namespace moe

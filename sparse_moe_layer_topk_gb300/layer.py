@@ -76,7 +76,7 @@ class LatentMoELayer:
             "route": ws(M.MOE_OP_ROUTE_TOPK, T=T_, E=E),
             "permute": ws(M.MOE_OP_PERMUTE, T=T_, E=E),
             "gbwd": ws(M.MOE_OP_GROUPED_SWIGLU_BWD, T=R, k=1, f=f),
-            "sbwd": ws(M.MOE_OP_SHARED_SWIGLU_BWD, T=T_, f=f, S=S),
+            "sbwd": ws(M.MOE_OP_SHARED_SWIGLU_BWD, T=T_, l=l, f=f, S=S),
             "rbwd": ws(M.MOE_OP_ROUTE_TOPK_BWD, T=T_, E=E),
         }
         self.ws = {n: torch.empty(max(b, 256), dtype=torch.uint8, device=dev)

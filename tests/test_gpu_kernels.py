@@ -259,7 +259,8 @@ def test_grouped_swiglu_fwd_bwd(counts, l, f):
             assert not dW13[e].any() and not dW2[e].any()
 
 
-@pytest.mark.parametrize("T,l,f,S", [(256, 128, 64, 1), (1000, 1024, 512, 2), (77, 256, 128, 3)])
+@pytest.mark.parametrize("T,l,f,S", [(256, 128, 64, 1), (1000, 1024, 512, 2), (77, 256, 128, 3),
+                                     (4096, 1024, 512, 2)])
 def test_shared_swiglu_fwd_bwd(T, l, f, S):
     z = _bf16(30, T, l)
     W13 = _bf16(31, S, l, 2 * f, std=0.02)
@@ -272,7 +273,7 @@ def test_shared_swiglu_fwd_bwd(T, l, f, S):
     dz = torch.empty(T, l, dtype=torch.bfloat16, device="cuda")
     dW13 = torch.empty(S, l, 2 * f, dtype=torch.float32, device="cuda")
     dW2 = torch.empty(S, f, l, dtype=torch.float32, device="cuda")
-    wsb = M.moe_workspace_size(M.MOE_OP_SHARED_SWIGLU_BWD, T=T, f=f, S=S)
+    wsb = M.moe_workspace_size(M.MOE_OP_SHARED_SWIGLU_BWD, T=T, l=l, f=f, S=S)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     M.moe_shared_swiglu_bwd(dev(dy), dev(z), dev(W13), dev(W2), gu, h, T, l, f, S, dz, dW13, dW2,
                             M.MOE_DTYPE_F32, ws, wsb)
