@@ -367,16 +367,18 @@ def run_ours(args):
     for name, (cnt, tot) in sorted(per_kernel.items(), key=lambda kv: -kv[1][1]):
         fl, by = work.get(name, (0, 0))
         avg_s = tot / cnt / 1000.0
+        floor_s = max(fl / (tc * 1e12), by / (hbm * 1e9))
         breakdown[name] = {"launches": cnt, "avg_us": round(avg_s * 1e6, 2),
                            "share": round(tot / sum(v[1] for v in per_kernel.values()), 4),
                            "tflops": round(fl / avg_s / 1e12, 1) if fl else None,
-                           "gbs": round(by / avg_s / 1e9, 1)}
+                           "gbs": round(by / avg_s / 1e9, 1),
+                           "roofline_frac": round(floor_s / avg_s, 3) if floor_s else None}
     if top:
         name, (cnt, tot) = top
         fl, by = work.get(name, (0, 0))
         avg_s = tot / cnt / 1000.0
-        ridge = tc * 1e12 / (hbm * 1e9)
-        if fl and fl / max(by, 1) >= ridge * 0.25:
+        # the bound is whichever of compute time and memory time is larger
+        if fl and fl / (tc * 1e12) >= by / (hbm * 1e9):
             roof = {"kernel": name, "bound": "tensor", "achieved": fl / avg_s / 1e12,
                     "peak": tc, "unit": "TFLOP/s", "frac": fl / avg_s / 1e12 / tc}
         else:

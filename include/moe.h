@@ -176,6 +176,19 @@ int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16
                        int E, int R, int l, int f, uint16_t* gu_save, uint16_t* h,
                        uint16_t* y_perm, void* stream);
 
+/* moe_grouped_swiglu with the permute fused into GEMM1's operand load: the
+ * permuted rows are never written. z is the unpermuted latent [T][l] and
+ * permuted row r is z[token_of[r]] (token_of from moe_permute, which can then
+ * be called with z = NULL); the TMA engine gathers the rows four at a time
+ * (tile::gather4) straight into the swizzled shared-memory tile. Results are
+ * identical to moe_permute + moe_grouped_swiglu. This is the "less data
+ * movement during token reordering" direction of [OPS]. */
+int moe_grouped_swiglu_gather(const uint16_t* z, const int32_t* token_of, int T,
+                              const uint16_t* W13, const uint16_t* W2, const int32_t* offsets,
+                              const int32_t* tile_sched, const float* row_w, int E, int R, int l,
+                              int f, uint16_t* gu_save, uint16_t* h, uint16_t* y_perm,
+                              void* stream);
+
 /* Shared experts of [MODEL] on all T latent rows, weight 1:
  *   [g_s|u_s] = z @ W13_sh[s];  h[:, s*f:(s+1)*f] = silu(g_s) * u_s   (h: bf16 [T][S*f])
  *   y_sh = sum_s h_s @ W2_sh[s]  (bf16 [T][l]);  gu_save: bf16 [T][S*2f], block s
@@ -219,6 +232,19 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
                            int E, int R, int l, int f, uint16_t* dz_perm, float* d_row_w,
                            void* dW13, void* dW2, int wgrad_dtype, void* ws, size_t ws_bytes,
                            void* stream);
+
+/* moe_grouped_swiglu_bwd with both permutes fused into the operand loads:
+ * dy_perm[r] = dy_lat[token_of[r]] and z_perm[r] = z[token_of[r]] are gathered
+ * by TMA inside the dgrad and wgrad GEMMs (dy_lat, z: [T][l]), so neither the
+ * combine backward gather nor the permuted activations are materialised.
+ * Results are identical to moe_grouped_swiglu_bwd on the permuted tensors. */
+int moe_grouped_swiglu_bwd_gather(const uint16_t* dy_lat, const uint16_t* z,
+                                  const int32_t* token_of, int T, const uint16_t* W13,
+                                  const uint16_t* W2, const uint16_t* gu_save, const uint16_t* h,
+                                  const float* row_w, const int32_t* offsets,
+                                  const int32_t* tile_sched, int E, int R, int l, int f,
+                                  uint16_t* dz_perm, float* d_row_w, void* dW13, void* dW2,
+                                  int wgrad_dtype, void* ws, size_t ws_bytes, void* stream);
 
 /* Backward of moe_shared_swiglu for dy = d loss / d y_sh ([T][l]):
  *   dz_sh = sum_s [dg_s|du_s] @ W13_sh[s]^T (bf16 [T][l]); dW13_sh [S][l][2f];

@@ -49,6 +49,10 @@ SIGNATURES = {
     "moe_latent_proj": ([_P, _P, _I, _I, _I, _P, _P], _I),
     "moe_latent_proj_bwd": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P], _I),
     "moe_grouped_swiglu": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_grouped_swiglu_gather": ([_P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P],
+                                  _I),
+    "moe_grouped_swiglu_bwd_gather": ([_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                       _P, _P, _P, _P, _I, _P, _Z, _P], _I),
     "moe_shared_swiglu": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_unpermute_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_unpermute_combine_bwd": ([_P, _P, _I, _I, _I, _P, _P], _I),
@@ -174,6 +178,20 @@ def moe_grouped_swiglu(z_perm, W13, W2, offsets, tile_sched, row_w, E, R, l, f, 
                        y_perm, stream=None):
     _call("moe_grouped_swiglu", z_perm, W13, W2, offsets, tile_sched, row_w, E, R, l, f, gu_save,
           h, y_perm, stream)
+
+
+def moe_grouped_swiglu_gather(z, token_of, T, W13, W2, offsets, tile_sched, row_w, E, R, l, f,
+                              gu_save, h, y_perm, stream=None):
+    _call("moe_grouped_swiglu_gather", z, token_of, T, W13, W2, offsets, tile_sched, row_w, E, R,
+          l, f, gu_save, h, y_perm, stream)
+
+
+def moe_grouped_swiglu_bwd_gather(dy_lat, z, token_of, T, W13, W2, gu_save, h, row_w, offsets,
+                                  tile_sched, E, R, l, f, dz_perm, d_row_w, dW13, dW2, wgrad_dtype,
+                                  ws, ws_bytes, stream=None):
+    _call("moe_grouped_swiglu_bwd_gather", dy_lat, z, token_of, T, W13, W2, gu_save, h, row_w,
+          offsets, tile_sched, E, R, l, f, dz_perm, d_row_w, dW13, dW2, wgrad_dtype, ws, ws_bytes,
+          stream)
 
 
 def moe_shared_swiglu(z, W13_sh, W2_sh, T, l, f, S, gu_save, h, y_sh, stream=None):

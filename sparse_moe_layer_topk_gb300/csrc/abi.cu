@@ -274,10 +274,16 @@ int moe_latent_proj_bwd(const uint16_t* dout, const uint16_t* in, const uint16_t
 
 // ---------------------------------------------------------------- experts
 
-int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16_t* W2,
-                       const int32_t* offsets, const int32_t* tile_sched, const float* row_w,
-                       int E, int R, int l, int f, uint16_t* gu_save, uint16_t* h,
-                       uint16_t* y_perm, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Grouped SwiGLU experts; A rows come from z_src ([src_rows][l]): permuted row r
+// is z_src row gather[r] when gather is given, else row r.
+int grouped_swiglu_impl(const uint16_t* z_perm, long long src_rows, const int32_t* gather,
+                        const uint16_t* W13, const uint16_t* W2, const int32_t* offsets,
+                        const int32_t* tile_sched, const float* row_w, int E, int R, int l, int f,
+                        uint16_t* gu_save, uint16_t* h, uint16_t* y_perm, void* stream) {
   MOE_REQUIRE(z_perm && W13 && W2 && offsets && tile_sched && h && y_perm, MOE_ERR_ARG);
   MOE_REQUIRE(E > 0 && R >= 0 && l > 0 && f > 0, MOE_ERR_ARG);
   MOE_REQUIRE(l % 64 == 0 && f % 64 == 0, MOE_ERR_ALIGN);
@@ -297,8 +303,10 @@ int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16
   L1.R_cap = R;
   L1.N = f;
   L1.K = l;
-  L1.A = view(z_perm, R, l, l);
+  L1.A = view(z_perm, src_rows, l, l);
   L1.a_mn = 0;
+  L1.gather_idx = gather;
+  L1.gather_a = gather != nullptr;
   L1.B = view(W13, l, 2ll * f, 2ll * f, E, static_cast<long long>(l) * 2 * f);
   L1.b_mn = 1;
   L1.b_batch_mode = BATCH_GROUP;
@@ -332,6 +340,28 @@ int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16
   L2.C = y_perm;
   L2.ldc = l;
   return gemm_launch(L2, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16_t* W2,
+                       const int32_t* offsets, const int32_t* tile_sched, const float* row_w,
+                       int E, int R, int l, int f, uint16_t* gu_save, uint16_t* h,
+                       uint16_t* y_perm, void* stream) {
+  return grouped_swiglu_impl(z_perm, R, nullptr, W13, W2, offsets, tile_sched, row_w, E, R, l, f,
+                             gu_save, h, y_perm, stream);
+}
+
+int moe_grouped_swiglu_gather(const uint16_t* z, const int32_t* token_of, int T,
+                              const uint16_t* W13, const uint16_t* W2, const int32_t* offsets,
+                              const int32_t* tile_sched, const float* row_w, int E, int R, int l,
+                              int f, uint16_t* gu_save, uint16_t* h, uint16_t* y_perm,
+                              void* stream) {
+  MOE_REQUIRE(token_of != nullptr && T > 0, MOE_ERR_ARG);
+  return grouped_swiglu_impl(z, T, token_of, W13, W2, offsets, tile_sched, row_w, E, R, l, f,
+                             gu_save, h, y_perm, stream);
 }
 
 int moe_shared_swiglu(const uint16_t* z, const uint16_t* W13_sh, const uint16_t* W2_sh, int T,
@@ -404,12 +434,18 @@ int moe_permute_bwd(const uint16_t* dz_perm, const int32_t* slot_of, const uint1
 
 // ---------------------------------------------------------------- backward
 
-int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, const uint16_t* W13,
-                           const uint16_t* W2, const uint16_t* gu_save, const uint16_t* h,
-                           const float* row_w, const int32_t* offsets, const int32_t* tile_sched,
-                           int E, int R, int l, int f, uint16_t* dz_perm, float* d_row_w,
-                           void* dW13, void* dW2, int wgrad_dtype, void* ws, size_t ws_bytes,
-                           void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Backward of the grouped experts; dy and z rows come from [src_rows][l]
+// sources, permuted row r being source row gather[r] when gather is given.
+int grouped_swiglu_bwd_impl(const uint16_t* dy_perm, const uint16_t* z_perm, long long src_rows,
+                            const int32_t* gather, const uint16_t* W13, const uint16_t* W2,
+                            const uint16_t* gu_save, const uint16_t* h, const float* row_w,
+                            const int32_t* offsets, const int32_t* tile_sched, int E, int R, int l,
+                            int f, uint16_t* dz_perm, float* d_row_w, void* dW13, void* dW2,
+                            int wgrad_dtype, void* ws, size_t ws_bytes, void* stream) {
   MOE_REQUIRE(dy_perm && z_perm && W13 && W2 && h && offsets && tile_sched && dz_perm && d_row_w &&
                   dW13 && dW2,
               MOE_ERR_ARG);
@@ -445,7 +481,9 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
   D2.R_cap = R;
   D2.N = f;
   D2.K = l;
-  D2.A = view(dy_perm, R, l, l);
+  D2.A = view(dy_perm, src_rows, l, l);
+  D2.gather_idx = gather;
+  D2.gather_a = gather != nullptr;
   D2.B = view(W2, f, l, l, E, static_cast<long long>(f) * l);  // B[n=f][k=l], K-major
   D2.b_mn = 0;
   D2.b_batch_mode = BATCH_GROUP;
@@ -475,8 +513,10 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
   W2g.N = l;
   W2g.A = view(hw, R, f, f);
   W2g.a_mn = 1;
-  W2g.B = view(dy_perm, R, l, l);
+  W2g.B = view(dy_perm, src_rows, l, l);
   W2g.b_mn = 1;
+  W2g.gather_idx = gather;
+  W2g.gather_b = gather != nullptr;
   W2g.epi = EPI_STORE;
   W2g.C = dW2;
   W2g.ldc = l;
@@ -512,8 +552,10 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
   W1g.offsets = offsets;
   W1g.M = l;
   W1g.N = 2 * f;
-  W1g.A = view(z_perm, R, l, l);
+  W1g.A = view(z_perm, src_rows, l, l);
   W1g.a_mn = 1;
+  W1g.gather_idx = gather;
+  W1g.gather_a = gather != nullptr;
   W1g.B = view(dgu, R, 2ll * f, 2ll * f);
   W1g.b_mn = 1;
   W1g.epi = EPI_STORE;
@@ -522,6 +564,34 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
   W1g.c_batch_stride = static_cast<long long>(l) * 2 * f;
   W1g.c_bf16 = wbf16;
   return gemm_launch(W1g, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, const uint16_t* W13,
+                           const uint16_t* W2, const uint16_t* gu_save, const uint16_t* h,
+                           const float* row_w, const int32_t* offsets, const int32_t* tile_sched,
+                           int E, int R, int l, int f, uint16_t* dz_perm, float* d_row_w,
+                           void* dW13, void* dW2, int wgrad_dtype, void* ws, size_t ws_bytes,
+                           void* stream) {
+  return grouped_swiglu_bwd_impl(dy_perm, z_perm, R, nullptr, W13, W2, gu_save, h, row_w, offsets,
+                                 tile_sched, E, R, l, f, dz_perm, d_row_w, dW13, dW2, wgrad_dtype,
+                                 ws, ws_bytes, stream);
+}
+
+int moe_grouped_swiglu_bwd_gather(const uint16_t* dy_lat, const uint16_t* z,
+                                  const int32_t* token_of, int T, const uint16_t* W13,
+                                  const uint16_t* W2, const uint16_t* gu_save, const uint16_t* h,
+                                  const float* row_w, const int32_t* offsets,
+                                  const int32_t* tile_sched, int E, int R, int l, int f,
+                                  uint16_t* dz_perm, float* d_row_w, void* dW13, void* dW2,
+                                  int wgrad_dtype, void* ws, size_t ws_bytes, void* stream) {
+  MOE_REQUIRE(token_of != nullptr && T > 0, MOE_ERR_ARG);
+  return grouped_swiglu_bwd_impl(dy_lat, z, T, token_of, W13, W2, gu_save, h, row_w, offsets,
+                                 tile_sched, E, R, l, f, dz_perm, d_row_w, dW13, dW2, wgrad_dtype,
+                                 ws, ws_bytes, stream);
 }
 
 int moe_shared_swiglu_bwd(const uint16_t* dy, const uint16_t* z, const uint16_t* W13_sh,

@@ -113,6 +113,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint6
       : "memory");
 }
 
+// Four rows of a 2-D tensor (box of one row) gathered by row index into four
+// consecutive 128-byte rows of shared memory (sm_100 tile::gather4 mode).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, uint64_t* bar, int col,
+                                            int4 rows) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(col), "r"(rows.x), "r"(rows.y),
+      "r"(rows.z), "r"(rows.w)
+      : "memory");
+}
+
 // TMA tensor store from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

@@ -79,6 +79,12 @@ struct GemmLaunch {
   // writes C. Deterministic (fixed summation order).
   int splitk = 1;
   float* splitk_ws = nullptr;
+  // Row gather (TMA tile::gather4): with gather_a (gather_b) the A (B) view is
+  // an unpermuted source tensor and permuted row r is its row gather_idx[r].
+  // Supported for the K-major A of a grouped-M GEMM and for one MN-major
+  // operand of a grouped-K GEMM.
+  const int* gather_idx = nullptr;
+  int gather_a = 0, gather_b = 0;
 };
 
 // Bytes of split workspace gemm_launch needs for M x N with `splitk` slices.

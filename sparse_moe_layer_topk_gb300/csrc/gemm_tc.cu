@@ -46,7 +46,7 @@ struct Cfg {
   static constexpr int STAGES = (BN == 256) ? (EW == 8 ? 3 : 4) : (EW == 8 ? 5 : 6);
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int THREADS = 64 + 32 * EW;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * 6144 + 1024 + 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * 6144 + 1024 + 1024;
 };
 
 struct Params {
@@ -74,6 +74,10 @@ struct Params {
   int dw_nparts;
   int* err_flag;
   int c0_rank3;  // the C store map is 3-D (grouped-K groups or column batches)
+  // Row gather: permuted row r of the gathered operand is row gather_idx[r] of its
+  // (unpermuted) source tensor, loaded with TMA tile::gather4.
+  const int* gather_idx;
+  int gather_a, gather_b;
 };
 
 struct Tile {
@@ -163,57 +167,106 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* err_f
 
 // ------------------------------------------------------------------ producer
 
-template <int BN, int EW>
+template <int BN, int EW, bool WARP>
 __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                              uint8_t* smem, uint64_t* full, uint64_t* empty,
+                              uint8_t* smem, uint64_t* full, uint64_t* empty, int* sidx,
                               volatile int* abort_flag) {
+  // WARP: run by the whole warp (the lanes fetch gather indices and issue the
+  // gather4 copies, lane 0 the others); otherwise by lane 0 alone.
   using C = Cfg<BN, EW>;
+  const uint32_t lane = WARP ? lane_id() : 0u;
   int stage = 0;
   uint32_t phase = 0;
   long long issued = 0;
   const int total = total_tiles(p);
+  const bool gather_m = WARP && p.gather_a && p.sched == SCHED_GROUPED_M;
+  const bool gather_k = WARP && (p.gather_a || p.gather_b) && p.sched == SCHED_GROUPED_K;
   bool ok = true;
   for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
     const Tile ti = decode<BN>(p, t);
+    if (gather_m) {
+      // source rows of the tile's 128 A rows; rows past the expert's segment
+      // repeat its last row (their results are never stored)
+      const int last = ti.m0 + ti.rows - 1;
+      __syncwarp();
+      for (int i = lane; i < BM; i += 32) sidx[i] = __ldg(p.gather_idx + min(ti.m0 + i, last));
+      __syncwarp();
+    }
     for (int kb = 0; kb < ti.nk; ++kb) {
-      if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-        raise_abort(abort_flag, p.err_flag);
+      int okw = 1;
+      if (lane == 0) okw = mbar_wait(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
+      if (WARP) okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+      if (!okw) {
+        if (lane == 0) raise_abort(abort_flag, p.err_flag);
         ok = false;
         break;
       }
+      const int k = ti.k0 + kb * BK;
+      if (gather_k) {
+        // source rows of this block's 64 K rows (rows past the segment are zeroed
+        // in shared memory before the MMA; any valid row will do for them)
+        const int last = ti.k0 + ti.krows - 1;
+        __syncwarp();
+        for (int i = lane; i < BK; i += 32) sidx[i] = __ldg(p.gather_idx + min(k + i, last));
+        __syncwarp();
+      }
       const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
       const uint32_t sB = sA + A_BYTES;
-      mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-      const int k = ti.k0 + kb * BK;
-      // A
-      if (!p.a_mn) {
-        tma_load_2d(sA, mapA, &full[stage], k, ti.m0);
-      } else {
-        tma_load_2d(sA, mapA, &full[stage], ti.m0, k);
-        tma_load_2d(sA + CHUNK_BYTES, mapA, &full[stage], ti.m0 + 64, k);
-      }
-      // B
-      int kb_coord = k, batch = ti.batch;
-      if (p.b_batch_mode == BATCH_FROM_K) {
-        batch = k / p.k_per_batch;
-        kb_coord = k - batch * p.k_per_batch;
-      }
-      if (!p.b_mn) {
-        if (p.b_rank3) tma_load_3d(sB, mapB, &full[stage], kb_coord, ti.nb0, batch);
-        else tma_load_2d(sB, mapB, &full[stage], kb_coord, ti.nb0);
-      } else {
+      const int4* gi = reinterpret_cast<const int4*>(sidx);
+      // Gathered operands: each lane issues its own gather4 copies (the
+      // barrier's expected bytes are posted by lane 0; the phase cannot complete
+      // before that arrival, so the order of the two does not matter).
+      if (gather_m) {
+        tma_gather4(sA + lane * 512, mapA, &full[stage], k, gi[lane]);  // 32 groups of 4 rows
+      } else if (gather_k && p.gather_a) {
+        const int c = lane >> 4, g = lane & 15;
+        tma_gather4(sA + c * CHUNK_BYTES + g * 512, mapA, &full[stage], ti.m0 + 64 * c, gi[g]);
+      } else if (gather_k && p.gather_b) {
 #pragma unroll
-        for (int c = 0; c < BN / 64; ++c) {
-          int ncoord;
-          if (p.swiglu_b) {
-            ncoord = (c < BN / 128) ? ti.nb0 + 64 * c : p.f + ti.nb0 + 64 * (c - BN / 128);
-          } else {
-            ncoord = ti.nb0 + 64 * c;
-          }
-          if (p.b_rank3) tma_load_3d(sB + c * CHUNK_BYTES, mapB, &full[stage], ncoord, kb_coord, batch);
-          else tma_load_2d(sB + c * CHUNK_BYTES, mapB, &full[stage], ncoord, kb_coord);
+        for (int i = 0; i < BN / 128; ++i) {
+          const int cg = lane + 32 * i;
+          const int c = cg >> 4, g = cg & 15;
+          tma_gather4(sB + c * CHUNK_BYTES + g * 512, mapB, &full[stage], ti.nb0 + 64 * c, gi[g]);
         }
       }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+        // A
+        if (!p.a_mn) {
+          if (!gather_m) tma_load_2d(sA, mapA, &full[stage], k, ti.m0);
+        } else if (!(gather_k && p.gather_a)) {
+          tma_load_2d(sA, mapA, &full[stage], ti.m0, k);
+          tma_load_2d(sA + CHUNK_BYTES, mapA, &full[stage], ti.m0 + 64, k);
+        }
+        // B
+        int kb_coord = k, batch = ti.batch;
+        if (p.b_batch_mode == BATCH_FROM_K) {
+          batch = k / p.k_per_batch;
+          kb_coord = k - batch * p.k_per_batch;
+        }
+        if (!p.b_mn) {
+          if (p.b_rank3) tma_load_3d(sB, mapB, &full[stage], kb_coord, ti.nb0, batch);
+          else tma_load_2d(sB, mapB, &full[stage], kb_coord, ti.nb0);
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) {
+            int ncoord;
+            if (p.swiglu_b) {
+              ncoord = (c < BN / 128) ? ti.nb0 + 64 * c : p.f + ti.nb0 + 64 * (c - BN / 128);
+            } else {
+              ncoord = ti.nb0 + 64 * c;
+            }
+            if (gather_k && p.gather_b) {
+              // issued lane-parallel above
+            } else if (p.b_rank3) {
+              tma_load_3d(sB + c * CHUNK_BYTES, mapB, &full[stage], ncoord, kb_coord, batch);
+            } else {
+              tma_load_2d(sB + c * CHUNK_BYTES, mapB, &full[stage], ncoord, kb_coord);
+            }
+          }
+        }
+      }
+      if (WARP) __syncwarp();
       ++issued;
       if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
     }
@@ -221,13 +274,16 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
   if (ok) {
     // Tail: wait until the MMA warp released every stage, so that no
     // tcgen05.commit arrival reaches this CTA's barriers after it exits.
-    for (int i = 0; i < C::STAGES; ++i) {
-      if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-        raise_abort(abort_flag, p.err_flag);
-        break;
+    if (lane == 0) {
+      for (int i = 0; i < C::STAGES; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+          raise_abort(abort_flag, p.err_flag);
+          break;
+        }
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
       }
-      if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
     }
+    if (WARP) __syncwarp();
   } else {
     // Wait (bounded, ignoring the abort flag) for the copies still in flight so
     // that none lands in shared memory after the CTA exits.
@@ -667,6 +723,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* sidx = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 256);  // 128 gather indices
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -694,7 +751,12 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane_id() == 0) producer_loop<BN, EW>(p, &mapA, &mapB, smem, full, empty, abort_flag);
+    // Gathering launches run the producer on the whole warp (the lanes fetch
+    // indices and issue gather4 copies); the others on lane 0 alone.
+    if (p.gather_a || p.gather_b) producer_loop<BN, EW, true>(p, &mapA, &mapB, smem, full, empty,
+                                                              sidx, abort_flag);
+    else if (lane_id() == 0) producer_loop<BN, EW, false>(p, &mapA, &mapB, smem, full, empty,
+                                                          sidx, abort_flag);
   } else if (warp == 1) {
     mma_loop<BN, EW>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
   } else {
@@ -816,14 +878,26 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   p.dw_part = L.dw_part;
   p.dw_nparts = L.dw_nparts;
   p.err_flag = L.err_flag;
+  p.gather_idx = L.gather_idx;
+  p.gather_a = L.gather_a;
+  p.gather_b = L.gather_b;
+  if (L.gather_a || L.gather_b) {
+    // supported: K-major A of a grouped-M GEMM, MN-major A or B of a grouped-K GEMM
+    const bool okm = L.sched == SCHED_GROUPED_M && L.gather_a && !L.gather_b && !L.a_mn;
+    const bool okk = L.sched == SCHED_GROUPED_K && (L.gather_a ? L.a_mn : 1) &&
+                     (L.gather_b ? L.b_mn : 1) && !(L.gather_a && L.gather_b);
+    if (!L.gather_idx || !(okm || okk) || (L.gather_b && (b3 || L.swiglu_b)))
+      return MOE_ERR_UNSUPPORTED;
+  }
   if (upper <= 0) return MOE_OK;
 
   if (!get_encoder()) return MOE_ERR_CUDA;
   CUtensorMap mapA, mapB, mapC0, mapC1;
   memset(&mapC0, 0, sizeof(mapC0));
   memset(&mapC1, 0, sizeof(mapC1));
-  if (!make_map(&mapA, L.A, L.a_mn ? 64 : BM, false)) return MOE_ERR_ARG;
-  if (!make_map(&mapB, L.B, L.b_mn ? 64 : BN, b3)) return MOE_ERR_ARG;
+  // gathered operands are read one row per box (tile::gather4)
+  if (!make_map(&mapA, L.A, L.gather_a ? 1 : (L.a_mn ? 64 : BM), false)) return MOE_ERR_ARG;
+  if (!make_map(&mapB, L.B, L.gather_b ? 1 : (L.b_mn ? 64 : BN), b3)) return MOE_ERR_ARG;
   // output (store) maps
   const long long rows_out = (L.sched == SCHED_GROUPED_M) ? L.R_cap : L.M;
   bool ok = true;

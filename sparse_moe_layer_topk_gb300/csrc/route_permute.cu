@@ -38,18 +38,26 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// Selection keys: (order-preserving bits of the value) << 32 | ~id, so a larger
+// key is a larger value or, for equal values, a lower expert id; 0 = no entry.
+__device__ __forceinline__ unsigned long long sel_key(float v, int e) {
+  return (static_cast<unsigned long long>(order_key(v)) << 32) |
+         static_cast<unsigned long long>(~static_cast<uint32_t>(e));
+}
+
 template <int NPL>
 __global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __restrict__ L,
-                                                           const float* __restrict__ bias, int T,
-                                                           int E, int k, int* __restrict__ idx,
-                                                           float* __restrict__ w_out,
-                                                           float* __restrict__ s_out,
-                                                           int* err_flag) {
+                                                              const float* __restrict__ bias,
+                                                              int T, int E, int k,
+                                                              int* __restrict__ idx,
+                                                              float* __restrict__ w_out,
+                                                              float* __restrict__ s_out,
+                                                              int* err_flag) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* row = L + static_cast<size_t>(t) * E;
-  uint32_t hi[NPL], lo[NPL];
+  unsigned long long key[NPL];
   bool bad = false;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
@@ -57,39 +65,44 @@ __global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __res
     if (e < E) {
       const float v = __ldg(row + e) + (bias ? __ldg(bias + e) : 0.0f);
       bad |= !isfinite(v);
-      hi[i] = order_key(v);
-      lo[i] = ~static_cast<uint32_t>(e);  // larger for the lower id
+      key[i] = sel_key(v, e);
     } else {
-      hi[i] = 0u;
-      lo[i] = 0u;
+      key[i] = 0ull;
     }
   }
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_flag(err_flag, MOE_FLAG_NONFINITE);
-  // local best (hi, lo) lexicographic
-  uint32_t bh = 0, bl = 0;
+  // this lane's largest and second largest key
+  unsigned long long b1 = 0ull, b2 = 0ull;
 #pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (hi[i] > bh || (hi[i] == bh && lo[i] > bl)) { bh = hi[i]; bl = lo[i]; }
-  float my_v = 0.0f;
-  int my_e = -1;
+  for (int i = 0; i < NPL; ++i) {
+    if (key[i] > b1) { b2 = b1; b1 = key[i]; } else if (key[i] > b2) { b2 = key[i]; }
+  }
+  bool has2 = true;
+  unsigned long long mine = 0ull;  // the j-th selection, kept by lane j
   for (int j = 0; j < k; ++j) {
-    const uint32_t mh = __reduce_max_sync(0xFFFFFFFFu, bh);
-    const uint32_t ml = __reduce_max_sync(0xFFFFFFFFu, bh == mh ? bl : 0u);
-    if (bh == mh && bl == ml) {  // the unique winner lane removes its entry
+    // warp-wide maximum key: high words first, then the low words of the lanes holding it
+    const uint32_t mh = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(b1 >> 32));
+    const uint32_t ml = __reduce_max_sync(
+        0xFFFFFFFFu, static_cast<uint32_t>(b1 >> 32) == mh ? static_cast<uint32_t>(b1) : 0u);
+    const unsigned long long m = (static_cast<unsigned long long>(mh) << 32) | ml;
+    if (lane == j) mine = m;
+    if (b1 == m) {
+      // The winner's keys at or above m are all taken (a lane always gives up its
+      // largest remaining key), so its next key is its second largest, or the
+      // largest key below m once the second has been used as well.
+      if (has2) {
+        b1 = b2;
+        has2 = false;
+      } else {
+        b1 = 0ull;
 #pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (hi[i] == mh && lo[i] == ml) { hi[i] = 0u; lo[i] = 0u; }
-      bh = 0;
-      bl = 0;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (hi[i] > bh || (hi[i] == bh && lo[i] > bl)) { bh = hi[i]; bl = lo[i]; }
-    }
-    if (lane == j) {
-      my_v = key_value(mh);
-      my_e = static_cast<int>(~ml);
+        for (int i = 0; i < NPL; ++i)
+          if (key[i] < m && key[i] > b1) b1 = key[i];
+      }
     }
   }
+  const float my_v = key_value(static_cast<uint32_t>(mine >> 32));
+  const int my_e = static_cast<int>(~static_cast<uint32_t>(mine));
   const float s = (lane < k) ? 1.0f / (1.0f + expf(-my_v)) : 0.0f;
   float sum = s;
 #pragma unroll

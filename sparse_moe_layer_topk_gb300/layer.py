@@ -9,6 +9,13 @@ Forward  (loss-free):  route_topk -> latent_proj(down) -> permute ->
 Backward (dout given): latent_proj_bwd(up) -> unpermute_combine_bwd ->
          grouped_swiglu_bwd -> shared_swiglu_bwd -> permute_bwd ->
          latent_proj_bwd(down) -> route_topk_bwd (adds the router's dx)
+
+With fused_gather the permute only builds the maps and the grouped GEMMs
+gather their permuted rows from z and dy_lat themselves
+(moe_grouped_swiglu[_bwd]_gather): z_perm and dy_perm are never written. It
+saves ~1 GB of activations at T=16384 but is slower on GB300 (the TMA gather4
+row loads run at a fraction of the tiled loads' rate), so the default is the
+explicit permute.
 """
 from __future__ import annotations
 
@@ -21,8 +28,9 @@ BF16 = torch.bfloat16
 
 class LatentMoELayer:
     def __init__(self, weights: dict, T: int, k: int, wgrad_dtype: int = M.MOE_DTYPE_F32,
-                 device="cuda"):
+                 device="cuda", fused_gather: bool = False):
         self.w = weights
+        self.fused_gather = fused_gather
         self.T = T
         self.k = k
         self.d, self.E = weights["Wr"].shape
@@ -46,7 +54,7 @@ class LatentMoELayer:
         self.slot_of = e(T_, k_, dt=torch.int32)
         self.token_of = e(R, dt=torch.int32)
         self.row_w = e(R, dt=torch.float32)
-        self.z_perm = e(R, l)
+        self.z_perm = None if fused_gather else e(R, l)
         self.gu = e(R, 2 * f)
         self.h = e(R, f)
         self.y_perm = e(R, l)
@@ -58,7 +66,7 @@ class LatentMoELayer:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         # backward
         self.dy_lat = e(T_, l)
-        self.dy_perm = e(R, l)
+        self.dy_perm = None if fused_gather else e(R, l)
         self.dz_perm = e(R, l)
         self.d_row_w = e(R, dt=torch.float32)
         self.d_topk_w = e(T_, k_, dt=torch.float32)
@@ -90,11 +98,18 @@ class LatentMoELayer:
         M.moe_route_topk(x, w["Wr"], w.get("bias"), T, d, E, k, self.topk_idx, self.topk_w,
                          self.topk_s, self.ws["route"], self.ws_sizes["route"], self.err, stream)
         M.moe_latent_proj(x, w["W_dn"], T, d, l, self.z, stream)
-        M.moe_permute(self.z, self.topk_idx, self.topk_w, T, l, E, k, self.z_perm, self.counts,
-                      self.offsets, self.slot_of, self.token_of, self.tile_sched, self.row_w,
-                      self.ws["permute"], self.ws_sizes["permute"], self.err, stream)
-        M.moe_grouped_swiglu(self.z_perm, w["W13"], w["W2"], self.offsets, self.tile_sched,
-                             self.row_w, E, R, l, f, self.gu, self.h, self.y_perm, stream)
+        fused = self.fused_gather
+        M.moe_permute(None if fused else self.z, self.topk_idx, self.topk_w, T, l, E, k,
+                      self.z_perm, self.counts, self.offsets, self.slot_of, self.token_of,
+                      self.tile_sched, self.row_w, self.ws["permute"], self.ws_sizes["permute"],
+                      self.err, stream)
+        if fused:
+            M.moe_grouped_swiglu_gather(self.z, self.token_of, T, w["W13"], w["W2"], self.offsets,
+                                        self.tile_sched, self.row_w, E, R, l, f, self.gu, self.h,
+                                        self.y_perm, stream)
+        else:
+            M.moe_grouped_swiglu(self.z_perm, w["W13"], w["W2"], self.offsets, self.tile_sched,
+                                 self.row_w, E, R, l, f, self.gu, self.h, self.y_perm, stream)
         M.moe_shared_swiglu(self.z, w["W13_sh"], w["W2_sh"], T, l, f, S, self.gu_sh, self.h_sh,
                             self.y_sh, stream)
         M.moe_unpermute_combine(self.y_perm, self.slot_of, self.y_sh, T, k, l, self.y_lat, stream)
@@ -109,11 +124,18 @@ class LatentMoELayer:
         wd = self.wgrad_dtype
         M.moe_latent_proj_bwd(dout, self.y_lat, w["W_up"], T, l, d, self.dy_lat, g["W_up"], wd,
                               stream)
-        M.moe_unpermute_combine_bwd(self.dy_lat, self.token_of, T, k, l, self.dy_perm, stream)
-        M.moe_grouped_swiglu_bwd(self.dy_perm, self.z_perm, w["W13"], w["W2"], self.gu, self.h,
-                                 self.row_w, self.offsets, self.tile_sched, E, R, l, f,
-                                 self.dz_perm, self.d_row_w, g["W13"], g["W2"], wd,
-                                 self.ws["gbwd"], self.ws_sizes["gbwd"], stream)
+        if self.fused_gather:
+            M.moe_grouped_swiglu_bwd_gather(self.dy_lat, self.z, self.token_of, T, w["W13"],
+                                            w["W2"], self.gu, self.h, self.row_w, self.offsets,
+                                            self.tile_sched, E, R, l, f, self.dz_perm,
+                                            self.d_row_w, g["W13"], g["W2"], wd, self.ws["gbwd"],
+                                            self.ws_sizes["gbwd"], stream)
+        else:
+            M.moe_unpermute_combine_bwd(self.dy_lat, self.token_of, T, k, l, self.dy_perm, stream)
+            M.moe_grouped_swiglu_bwd(self.dy_perm, self.z_perm, w["W13"], w["W2"], self.gu,
+                                     self.h, self.row_w, self.offsets, self.tile_sched, E, R, l,
+                                     f, self.dz_perm, self.d_row_w, g["W13"], g["W2"], wd,
+                                     self.ws["gbwd"], self.ws_sizes["gbwd"], stream)
         M.moe_shared_swiglu_bwd(self.dy_lat, self.z, w["W13_sh"], w["W2_sh"], self.gu_sh,
                                 self.h_sh, T, l, f, S, self.dz_sh, g["W13_sh"], g["W2_sh"], wd,
                                 self.ws["sbwd"], self.ws_sizes["sbwd"], stream)

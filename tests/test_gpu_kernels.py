@@ -332,3 +332,49 @@ def test_host_argument_errors_do_not_launch():
         M.moe_latent_proj(x, x, 64, 64, 96, x)
     with pytest.raises(M.MoEError, match="workspace"):
         M.moe_route_topk(x, x, None, 64, 64, 64, 4, x, x, x, x, 16)
+
+
+@pytest.mark.parametrize("T,E,k,l,f,skew", [(300, 37, 4, 128, 64, 1.5), (2048, 64, 8, 1024, 512, 0.0),
+                                             (1, 16, 4, 256, 128, 0.0)])
+def test_gather_fused_grouped_gemms_equal_explicit_permute(T, E, k, l, f, skew):
+    """moe_grouped_swiglu[_bwd]_gather (rows gathered by TMA inside the GEMMs)
+    produce bit-identical results to the explicit permute followed by the
+    plain grouped calls: the same bytes land in the same shared-memory tiles."""
+    idx = I.make_topk_ids(50 + T, T, E, k, skew=skew)
+    z = _bf16(51, T, l)
+    dy_lat = _bf16(52, T, l)
+    tw = torch.rand(T, k, generator=torch.Generator().manual_seed(5)) * 0.2 + 0.01
+    g = _run_permute(idx, E, l, z, tw)
+    R = T * k
+    W13 = dev(_bf16(53, E, l, 2 * f, std=0.02))
+    W2 = dev(_bf16(54, E, f, l, std=0.02))
+    off, sch, tok, roww = (dev(g["offsets"]), dev(g["tile_sched"]), dev(g["token_of"]),
+                           dev(g["row_w"]))
+    outs = []
+    for fused in (False, True):
+        gu = torch.empty(R, 2 * f, dtype=torch.bfloat16, device="cuda")
+        h = torch.empty(R, f, dtype=torch.bfloat16, device="cuda")
+        y = torch.empty(R, l, dtype=torch.bfloat16, device="cuda")
+        dz = torch.empty(R, l, dtype=torch.bfloat16, device="cuda")
+        drw = torch.empty(R, dtype=torch.float32, device="cuda")
+        dW13 = torch.empty(E, l, 2 * f, dtype=torch.float32, device="cuda")
+        dW2 = torch.empty(E, f, l, dtype=torch.float32, device="cuda")
+        wsb = M.moe_workspace_size(M.MOE_OP_GROUPED_SWIGLU_BWD, T=R, k=1, f=f)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        if fused:
+            M.moe_grouped_swiglu_gather(dev(z), tok, T, W13, W2, off, sch, roww, E, R, l, f, gu, h,
+                                        y)
+            M.moe_grouped_swiglu_bwd_gather(dev(dy_lat), dev(z), tok, T, W13, W2, gu, h, roww, off,
+                                            sch, E, R, l, f, dz, drw, dW13, dW2, M.MOE_DTYPE_F32,
+                                            ws, wsb)
+        else:
+            dy_perm = torch.empty(R, l, dtype=torch.bfloat16, device="cuda")
+            M.moe_unpermute_combine_bwd(dev(dy_lat), tok, T, k, l, dy_perm)
+            M.moe_grouped_swiglu(dev(g["z_perm"]), W13, W2, off, sch, roww, E, R, l, f, gu, h, y)
+            M.moe_grouped_swiglu_bwd(dy_perm, dev(g["z_perm"]), W13, W2, gu, h, roww, off, sch, E,
+                                     R, l, f, dz, drw, dW13, dW2, M.MOE_DTYPE_F32, ws, wsb)
+        torch.cuda.synchronize()
+        outs.append([t.cpu() for t in (gu, h, y, dz, drw, dW13, dW2)])
+    for name, a, b in zip(("gu", "h", "y", "dz", "d_row_w", "dW13", "dW2"), *outs):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b), name
