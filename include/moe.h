@@ -77,6 +77,7 @@ extern "C" {
 #define MOE_OP_GROUPED_SWIGLU_BWD 3
 #define MOE_OP_SHARED_SWIGLU_BWD 4
 #define MOE_OP_ROUTE_TOPK_BWD 5
+#define MOE_OP_ROUTER_AUX 6
 
 int moe_version(void);
 const char* moe_status_string(int status);
@@ -108,6 +109,18 @@ int moe_topk_from_logits(const float* logits, const float* bias, int T, int E, i
 int moe_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int T, int d, int E,
                    int k, int32_t* topk_idx, float* topk_w, float* topk_s, void* ws,
                    size_t ws_bytes, int32_t* err_flag, void* stream);
+
+/* Auxiliary load-balance loss of the routing stage ("大模型落地昇腾" page, section
+ * "三、通信侧": an auxiliary loss that constrains the entropy of the routing
+ * distribution), read as the negative entropy of the batch's mean routing
+ * distribution over all experts:
+ *   P(e|t) = s[t][e] / sum_e' s[t][e'],  s = sigmoid(logits + bias)   (bias nullable)
+ *   p_mean[e] = (1/T) sum_t P(e|t)  (fp32, E);  loss = sum_e p_mean[e] ln p_mean[e]  (fp32, 1)
+ * The loss is -ln E when the routing mass is spread evenly. Deterministic
+ * (fixed-order reductions). Workspace: moe_workspace_size(MOE_OP_ROUTER_AUX, T, 0, 0, E, ...).
+ * Its gradient is added by moe_route_topk_bwd (aux_* arguments). */
+int moe_router_aux_loss(const float* logits, const float* bias, int T, int E, float* p_mean,
+                        float* loss, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- permute */
 
@@ -146,6 +159,21 @@ int moe_permute_noalloc(const uint16_t* z, const int32_t* topk_idx, const float*
                         int l, int E, int k, uint16_t* z_perm, int32_t* counts, int32_t* offsets,
                         int32_t* slot_of, int32_t* token_of, int32_t* tile_sched, float* row_w,
                         int32_t* err_flag, void* stream);
+
+/* Online load plan with dynamic expert replicas for an expert-parallel layout
+ * ("TorchTitan Ascend开源" page, sections "在线负载规划" and
+ * "MoonEP动态负载均衡与专家并行优化": per-expert loads of the current batch and
+ * each device's remaining capacity decide the replicas of hot experts; a token
+ * keeps its expert). Reading: P ranks, rank r owns experts [r*E/P, (r+1)*E/P)
+ * (E divisible by P), every rank processes at most C = ceil(sum counts / P)
+ * rows. Ranks first take their own experts' rows while they have room; the
+ * rest of each expert goes, in rank order, to ranks with spare capacity.
+ * Output: pieces[i][4] = {expert, rank, first row within the expert's
+ * segment, rows} for i < *n_pieces (capacity 2E + P pieces, int32),
+ * rank_load[P] = rows per rank (max = C). Runs on the device from the counts
+ * of moe_permute (no host synchronisation). E + P <= 2048. */
+int moe_replica_plan(const int32_t* counts, int E, int P, int32_t* pieces, int32_t* n_pieces,
+                     int32_t* rank_load, void* stream);
 
 /* ---------------------------------------------------------------- projections */
 
@@ -268,6 +296,10 @@ int moe_permute_bwd(const uint16_t* dz_perm, const int32_t* slot_of, const uint1
  *   ds_j = (d_topk_w_j - sum_i w_i d_topk_w_i) / sum_i s_i;  dL[t][idx_j] = ds_j s_j (1 - s_j),
  *   zero for unselected experts (the selection is piecewise constant; the bias
  *   is a constant and gets no gradient)
+ *   with aux_logits != NULL, dL also gets the gradient of aux_scale * the
+ *   auxiliary balance loss (moe_router_aux_loss on aux_logits + aux_bias, whose
+ *   p_mean is aux_p_mean): dense over all E experts,
+ *   dL[t][e] += aux_scale s(1-s) / (T S_t) (ln p_mean[e] - sum_e' P(e'|t) ln p_mean[e'])
  *   dx_accum[T][d] += dL @ Wr^T  (bf16, read-modify-write)
  *   dWr[d][E] = x^T @ dL         (fp32 or bf16)
  * E must be a multiple of 64. Workspace (dL in bf16):
@@ -275,8 +307,9 @@ int moe_permute_bwd(const uint16_t* dz_perm, const int32_t* slot_of, const uint1
 int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32_t* topk_idx,
                        const float* topk_w, const float* topk_s, const uint16_t* x,
                        const uint16_t* Wr, int T, int d, int E, int k, float* d_topk_w,
-                       uint16_t* dx_accum, void* dWr, int wgrad_dtype, void* ws, size_t ws_bytes,
-                       int32_t* err_flag, void* stream);
+                       uint16_t* dx_accum, void* dWr, int wgrad_dtype, const float* aux_logits,
+                       const float* aux_bias, const float* aux_p_mean, float aux_scale, void* ws,
+                       size_t ws_bytes, int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------- diagnostics */
 

@@ -21,6 +21,11 @@ Sources (the pages give the structure, not the formulas):
           dispatch, Permute / Unpermute / Grouped GEMM as the core operators.
   [MOE-D] "TorchTitan Ascend开源" page, section "在线负载规划": per-expert load
           counted from the current routing result.
+  [PLAN]  "TorchTitan Ascend开源" page, sections "在线负载规划" and
+          "MoonEP动态负载均衡与专家并行优化": online replica planning.
+  [AUX]   "大模型落地昇腾:从适配挑战到高效训练实践" page, section "三、通信侧":
+          an auxiliary load-balance loss that constrains the entropy of the
+          routing distribution.
 Readings where the pages are silent (router = sigmoid(x@Wr) with renormalised
 top-k weights, lower expert id wins ties, tokens of an expert in ascending
 token order, shared experts in latent space with weight 1, routing weight
@@ -40,6 +45,7 @@ __all__ = [
     "expert_offsets", "permutation_maps", "permute_rows", "swiglu_expert",
     "grouped_swiglu", "combine", "layer_forward", "layer_backward",
     "ep_rank_forward", "m_tiles_schedule", "router_backward", "swiglu_expert_backward",
+    "aux_balance_loss", "aux_balance_loss_backward", "replica_plan",
 ]
 
 
@@ -299,6 +305,93 @@ def router_backward(d_w, w, s, idx, E: int) -> np.ndarray:
     dL = np.zeros((d_w.shape[0], E))
     np.put_along_axis(dL, np.asarray(idx), ds * s * (1.0 - s), axis=1)
     return dL
+
+
+# --------------------------------------------------------------------------
+# Auxiliary load balance  [AUX]: "大模型落地昇腾" page, section "三、通信侧",
+# routing-aware token dispatch: an auxiliary loss at the routing stage that
+# constrains the entropy of the routing distribution.
+# --------------------------------------------------------------------------
+
+def aux_balance_loss(L, bias=None):
+    """Negative entropy of the batch's mean routing distribution.
+
+    P(e|t) = s[t,e] / sum_e' s[t,e'] with s = sigmoid(L + b) over all E experts
+    (the router's scores normalised per token); pbar_e = mean_t P(e|t);
+    loss = sum_e pbar_e log pbar_e = -H(pbar), smallest (-log E) when the
+    batch's routing mass is spread evenly. Returns (pbar [E], loss)."""
+    L = _f64(L)
+    if bias is not None:
+        L = L + _f64(bias)[None, :]
+    s = sigmoid(L)
+    P = s / s.sum(axis=1, keepdims=True)
+    pbar = P.mean(axis=0)
+    return pbar, float(np.sum(pbar * np.log(pbar)))
+
+
+def aux_balance_loss_backward(L, bias=None, scale: float = 1.0):
+    """d(scale * aux_balance_loss)/dL, dense [T,E]:
+    d/dP(e|t) = (log pbar_e + 1) / T; P = s / S gives
+    d/ds_j = (c_j - sum_e c_e P_e) / (T S) with c = log pbar (the +1 cancels
+    because sum_e P_e = 1); ds_j/dL_j = s_j (1 - s_j)."""
+    L = _f64(L)
+    if bias is not None:
+        L = L + _f64(bias)[None, :]
+    T = L.shape[0]
+    s = sigmoid(L)
+    S = s.sum(axis=1, keepdims=True)
+    P = s / S
+    c = np.log(P.mean(axis=0))[None, :]
+    inner = (c * P).sum(axis=1, keepdims=True)
+    return scale * s * (1.0 - s) * (c - inner) / (T * S)
+
+
+# --------------------------------------------------------------------------
+# Online load planning with dynamic replicas  [PLAN]: "TorchTitan Ascend开源" page,
+# sections "在线负载规划" and "MoonEP动态负载均衡与专家并行优化": per-expert
+# loads of the current batch plus each device's remaining capacity decide where
+# hot experts get replicas; tokens keep their expert; in the page's figure 32
+# unevenly spread tasks end as 4 on each of 8 ranks.
+# --------------------------------------------------------------------------
+
+def replica_plan(counts, P: int):
+    """Greedy plan of an expert-parallel layout: rank r owns experts
+    [r*E/P, (r+1)*E/P) (E divisible by P); every rank may process at most
+    C = ceil(sum(counts) / P) rows.
+
+    1. Each rank takes the rows of its own experts, in expert order, while it
+       has capacity.
+    2. The rows left over, expert by expert, go to ranks in rank order, each
+       taking as many as its spare capacity allows (a replica of the expert).
+    Returns (pieces, load): pieces = list of (expert, rank, first_row, n_rows)
+    with rows counted within the expert's segment, in the order they were
+    made; load[r] = rows rank r processes (max(load) = C)."""
+    counts = [int(c) for c in counts]
+    E = len(counts)
+    assert E % P == 0
+    per = E // P
+    R = sum(counts)
+    C = -(-R // P)
+    load = [0] * P
+    done = [0] * E
+    pieces = []
+    for r in range(P):
+        for e in range(r * per, (r + 1) * per):
+            take = min(counts[e], C - load[r])
+            if take > 0:
+                pieces.append((e, r, 0, take))
+                load[r] += take
+                done[e] = take
+    for e in range(E):
+        r = 0
+        while done[e] < counts[e]:
+            while load[r] >= C:
+                r += 1
+            take = min(counts[e] - done[e], C - load[r])
+            pieces.append((e, r, done[e], take))
+            load[r] += take
+            done[e] += take
+    return pieces, load
 
 
 def ep_rank_forward(z_perm, counts, W13, W2, w, perm):

@@ -30,10 +30,12 @@ MOE_OP_PERMUTE = 2
 MOE_OP_GROUPED_SWIGLU_BWD = 3
 MOE_OP_SHARED_SWIGLU_BWD = 4
 MOE_OP_ROUTE_TOPK_BWD = 5
+MOE_OP_ROUTER_AUX = 6
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _Z = ctypes.c_size_t
+_F = ctypes.c_float
 
 # name -> argument types (pointer args are _P; the last one is always the stream)
 SIGNATURES = {
@@ -61,8 +63,10 @@ SIGNATURES = {
     "moe_shared_swiglu_bwd": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _Z, _P],
                               _I),
     "moe_permute_bwd": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
-    "moe_route_topk_bwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _Z, _P,
-                            _P], _I),
+    "moe_route_topk_bwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P,
+                            _F, _P, _Z, _P, _P], _I),
+    "moe_router_aux_loss": ([_P, _P, _I, _I, _P, _P, _P, _Z, _P], _I),
+    "moe_replica_plan": ([_P, _I, _I, _P, _P, _P, _P], _I),
     "moe_timing_enable": ([_I], _I),
     "moe_timing_report": ([ctypes.c_char_p, _Z], _I),
 }
@@ -224,9 +228,15 @@ def moe_permute_bwd(dz_perm, slot_of, dz_shared, T, k, l, dz, stream=None):
 
 
 def moe_route_topk_bwd(d_row_w, slot_of, topk_idx, topk_w, topk_s, x, Wr, T, d, E, k, d_topk_w,
-                       dx_accum, dWr, wgrad_dtype, ws, ws_bytes, err_flag=None, stream=None):
+                       dx_accum, dWr, wgrad_dtype, aux_logits, aux_bias, aux_p_mean, aux_scale, ws,
+                       ws_bytes, err_flag=None, stream=None):
     _call("moe_route_topk_bwd", d_row_w, slot_of, topk_idx, topk_w, topk_s, x, Wr, T, d, E, k,
-          d_topk_w, dx_accum, dWr, wgrad_dtype, ws, ws_bytes, err_flag, stream)
+          d_topk_w, dx_accum, dWr, wgrad_dtype, aux_logits, aux_bias, aux_p_mean, float(aux_scale),
+          ws, ws_bytes, err_flag, stream)
+
+
+def moe_router_aux_loss(logits, bias, T, E, p_mean, loss, ws, ws_bytes, stream=None):
+    _call("moe_router_aux_loss", logits, bias, T, E, p_mean, loss, ws, ws_bytes, stream)
 
 
 def moe_timing_enable(on: bool):
@@ -244,3 +254,7 @@ def moe_timing_report() -> dict:
         name, cnt, ms = line.split()
         out[name] = (int(cnt), float(ms))
     return out
+
+
+def moe_replica_plan(counts, E, P, pieces, n_pieces, rank_load, stream=None):
+    _call("moe_replica_plan", counts, E, P, pieces, n_pieces, rank_load, stream)

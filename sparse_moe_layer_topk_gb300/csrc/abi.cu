@@ -168,6 +168,7 @@ size_t moe_workspace_size(int op, int T, int d, int l, int E, int k, int f, int 
       return grouped_bwd_ws(static_cast<long long>(T) * (k > 0 ? k : 1), f);
     case MOE_OP_SHARED_SWIGLU_BWD: return shared_bwd_ws(T, l, f, S);
     case MOE_OP_ROUTE_TOPK_BWD: return up256(static_cast<size_t>(T) * E * 2);
+    case MOE_OP_ROUTER_AUX: return up256(static_cast<size_t>(aux_partial_warps(T)) * E * 4);
     default: return 0;
   }
 }
@@ -209,6 +210,16 @@ int moe_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int
   return moe_topk_from_logits(L, bias, T, E, k, topk_idx, topk_w, topk_s, err_flag, stream);
 }
 
+int moe_router_aux_loss(const float* logits, const float* bias, int T, int E, float* p_mean,
+                        float* loss, void* ws, size_t ws_bytes, void* stream) {
+  MOE_REQUIRE(logits && p_mean && loss, MOE_ERR_ARG);
+  MOE_REQUIRE(T > 0 && E > 0 && E <= 1024, MOE_ERR_ARG);
+  MOE_REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_ROUTER_AUX, T, 0, 0, E, 0, 0, 0),
+              MOE_ERR_WORKSPACE);
+  return cuda_status(launch_aux_loss(logits, bias, T, E, reinterpret_cast<float*>(ws), p_mean, loss,
+                                     S(stream)));
+}
+
 // ---------------------------------------------------------------- permute
 
 int moe_permute(const uint16_t* z, const int32_t* topk_idx, const float* topk_w, int T, int l,
@@ -233,6 +244,13 @@ int moe_permute(const uint16_t* z, const int32_t* topk_idx, const float* topk_w,
   if (z) MOE_CHECK(cuda_status(launch_gather_rows("permute_gather", z, token_of, static_cast<long long>(T) * k, l,
                                                   z_perm, st)));
   return MOE_OK;
+}
+
+int moe_replica_plan(const int32_t* counts, int E, int P, int32_t* pieces, int32_t* n_pieces,
+                     int32_t* rank_load, void* stream) {
+  MOE_REQUIRE(counts && pieces && n_pieces && rank_load, MOE_ERR_ARG);
+  MOE_REQUIRE(E > 0 && P > 0 && E % P == 0 && E + P <= 2048, MOE_ERR_ARG);
+  return cuda_status(launch_replica_plan(counts, E, P, pieces, n_pieces, rank_load, S(stream)));
 }
 
 // ---------------------------------------------------------------- projections
@@ -704,8 +722,9 @@ int moe_shared_swiglu_bwd(const uint16_t* dy, const uint16_t* z, const uint16_t*
 int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32_t* topk_idx,
                        const float* topk_w, const float* topk_s, const uint16_t* x,
                        const uint16_t* Wr, int T, int d, int E, int k, float* d_topk_w,
-                       uint16_t* dx_accum, void* dWr, int wgrad_dtype, void* ws, size_t ws_bytes,
-                       int32_t* err_flag, void* stream) {
+                       uint16_t* dx_accum, void* dWr, int wgrad_dtype, const float* aux_logits,
+                       const float* aux_bias, const float* aux_p_mean, float aux_scale, void* ws,
+                       size_t ws_bytes, int32_t* err_flag, void* stream) {
   MOE_REQUIRE(d_row_w && slot_of && topk_idx && topk_w && topk_s, MOE_ERR_ARG);
   MOE_REQUIRE(T >= 0 && d > 0 && E > 0 && E <= 1024 && k >= 1 && k <= 32 && k <= E, MOE_ERR_ARG);
   MOE_REQUIRE(wgrad_dtype == MOE_DTYPE_F32 || wgrad_dtype == MOE_DTYPE_BF16, MOE_ERR_ARG);
@@ -725,6 +744,10 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
   uint16_t* dL = reinterpret_cast<uint16_t*>(ws);
   MOE_CHECK(cuda_status(launch_router_bwd(d_row_w, slot_of, topk_idx, topk_w, topk_s, T, E, k,
                                           d_topk_w, dL, err_flag, st)));
+  if (aux_logits) {
+    MOE_REQUIRE(aux_p_mean != nullptr, MOE_ERR_ARG);
+    MOE_CHECK(cuda_status(launch_aux_bwd(aux_logits, aux_bias, aux_p_mean, T, E, aux_scale, dL, st)));
+  }
   if (dx_accum) MOE_CHECK(dense_gemm("router_dgrad", dL, E, 0, Wr, E, 0, T, d, E, dx_accum, d, 1, 1, st));
   if (dWr)
     MOE_CHECK(dense_gemm("router_wgrad", x, d, 1, dL, E, 1, d, E, T, dWr, E, wgrad_dtype == MOE_DTYPE_BF16, 0, st));

@@ -25,4 +25,13 @@ cudaError_t launch_router_bwd(const float* d_row_w, const int* slot_of, const in
                               const float* topk_w, const float* topk_s, int T, int E, int k,
                               float* d_topk_w, void* dL, int* err_flag, cudaStream_t st);
 
+int aux_partial_warps(int T);
+cudaError_t launch_aux_loss(const float* L, const float* bias, int T, int E, float* part,
+                            float* p_mean, float* loss, cudaStream_t st);
+cudaError_t launch_aux_bwd(const float* L, const float* bias, const float* p_mean, int T, int E,
+                           float scale, void* dL, cudaStream_t st);
+
+cudaError_t launch_replica_plan(const int* counts, int E, int P, int* pieces, int* n_pieces,
+                                int* load, cudaStream_t st);
+
 }  // namespace moe

@@ -362,6 +362,118 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
   }
 }
 
+// ---- auxiliary balance loss: -H(pbar), pbar_e = mean_t s_te / sum_e' s_te'
+
+// Warp w sums P(e|t) over its token range [w*tpw, (w+1)*tpw) into part[w][e].
+template <int NPL>
+__global__ void __launch_bounds__(256) aux_partial_kernel(const float* __restrict__ L,
+                                                          const float* __restrict__ bias, int T,
+                                                          int E, int tpw, int nwarps,
+                                                          float* __restrict__ part) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= nwarps) return;
+  float acc[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) acc[i] = 0.0f;
+  const int t1 = min(T, (w + 1) * tpw);
+  for (int t = w * tpw; t < t1; ++t) {
+    const float* row = L + static_cast<size_t>(t) * E;
+    float sv[NPL];
+    float ssum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      sv[i] = 0.0f;
+      if (e < E) {
+        const float v = __ldg(row + e) + (bias ? __ldg(bias + e) : 0.0f);
+        sv[i] = 1.0f / (1.0f + expf(-v));
+        ssum += sv[i];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
+    const float inv = 1.0f / ssum;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) acc[i] = fmaf(sv[i], inv, acc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) part[static_cast<size_t>(w) * E + e] = acc[i];
+  }
+}
+
+// One CTA of 1024 threads: pbar_e = sum_w part[w][e] / T (in w order), loss = sum pbar log pbar.
+__global__ void __launch_bounds__(1024) aux_reduce_kernel(const float* __restrict__ part,
+                                                          int nwarps, int E, int T,
+                                                          float* __restrict__ p_mean,
+                                                          float* __restrict__ loss) {
+  __shared__ float red[32];
+  const int e = threadIdx.x;
+  float term = 0.0f;
+  if (e < E) {
+    float sum = 0.0f;
+    for (int w = 0; w < nwarps; ++w) sum += part[static_cast<size_t>(w) * E + e];
+    const float p = sum / static_cast<float>(T);
+    p_mean[e] = p;
+    term = p > 0.0f ? p * logf(p) : 0.0f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xFFFFFFFFu, term, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = term;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = red[threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if (threadIdx.x == 0) *loss = v;
+  }
+}
+
+// One warp per token: dL[t][e] += scale * s(1-s)/(T S) * (log pbar_e - sum_e' P_e' log pbar_e').
+template <int NPL>
+__global__ void __launch_bounds__(256) aux_bwd_kernel(const float* __restrict__ L,
+                                                      const float* __restrict__ bias,
+                                                      const float* __restrict__ p_mean, int T,
+                                                      int E, float scale, bf16* __restrict__ dL) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = L + static_cast<size_t>(t) * E;
+  float sv[NPL], cv[NPL];
+  float ssum = 0.0f, csum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    sv[i] = 0.0f;
+    cv[i] = 0.0f;
+    if (e < E) {
+      const float v = __ldg(row + e) + (bias ? __ldg(bias + e) : 0.0f);
+      sv[i] = 1.0f / (1.0f + expf(-v));
+      cv[i] = logf(__ldg(p_mean + e));
+      ssum += sv[i];
+      csum = fmaf(cv[i], sv[i], csum);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
+    csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o);
+  }
+  const float inner = csum / ssum;  // sum_e P_e log pbar_e
+  const float k0 = scale / (static_cast<float>(T) * ssum);
+  bf16* drow = dL + static_cast<size_t>(t) * E;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float g = k0 * sv[i] * (1.0f - sv[i]) * (cv[i] - inner);
+      drow[e] = __float2bfloat16_rn(__bfloat162float(drow[e]) + g);
+    }
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
@@ -446,6 +558,109 @@ cudaError_t launch_router_bwd(const float* d_row_w, const int* slot_of, const in
   router_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(d_row_w, slot_of, topk_idx, topk_w, topk_s, T, E,
                                                  k, d_topk_w, reinterpret_cast<bf16*>(dL),
                                                  err_flag);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
+
+namespace moe {
+
+int aux_partial_warps(int T) {
+  const int w = (T + 15) / 16;
+  return w < 1024 ? (w < 1 ? 1 : w) : 1024;
+}
+
+#define MOE_AUX_DISPATCH(KERNEL, GRID, ...)                                   \
+  do {                                                                         \
+    const int npl_ = (E + 31) / 32;                                            \
+    if (npl_ <= 2) KERNEL<2><<<GRID, 256, 0, st>>>(__VA_ARGS__);               \
+    else if (npl_ <= 4) KERNEL<4><<<GRID, 256, 0, st>>>(__VA_ARGS__);          \
+    else if (npl_ <= 8) KERNEL<8><<<GRID, 256, 0, st>>>(__VA_ARGS__);          \
+    else if (npl_ <= 16) KERNEL<16><<<GRID, 256, 0, st>>>(__VA_ARGS__);        \
+    else if (npl_ <= 28) KERNEL<28><<<GRID, 256, 0, st>>>(__VA_ARGS__);        \
+    else KERNEL<32><<<GRID, 256, 0, st>>>(__VA_ARGS__);                        \
+  } while (0)
+
+cudaError_t launch_aux_loss(const float* L, const float* bias, int T, int E, float* part,
+                            float* p_mean, float* loss, cudaStream_t st) {
+  const int nw = aux_partial_warps(T);
+  const int tpw = (T + nw - 1) / nw;
+  {
+    LaunchTimer lt("router_aux_partial", st);
+    MOE_AUX_DISPATCH(aux_partial_kernel, (nw + 7) / 8, L, bias, T, E, tpw, nw, part);
+  }
+  {
+    LaunchTimer lt("router_aux_reduce", st);
+    aux_reduce_kernel<<<1, 1024, 0, st>>>(part, nw, E, T, p_mean, loss);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_aux_bwd(const float* L, const float* bias, const float* p_mean, int T, int E,
+                           float scale, void* dL, cudaStream_t st) {
+  LaunchTimer lt("router_aux_bwd", st);
+  MOE_AUX_DISPATCH(aux_bwd_kernel, (T + 7) / 8, L, bias, p_mean, T, E, scale,
+                   reinterpret_cast<bf16*>(dL));
+  return cudaGetLastError();
+}
+
+}  // namespace moe
+
+namespace moe {
+namespace {
+
+// Online replica plan (one thread; E + P <= 2048 steps): rank r owns experts
+// [r*E/P, (r+1)*E/P) and may process C = ceil(rows / P) rows. Ranks first take
+// their own experts' rows while they have room; the rest of each expert goes,
+// in rank order, to ranks with spare capacity (replicas that keep the expert).
+// pieces[i] = {expert, rank, first row within the expert's segment, rows}.
+__global__ void replica_plan_kernel(const int* __restrict__ counts, int E, int P,
+                                    int* __restrict__ pieces, int* __restrict__ n_pieces,
+                                    int* __restrict__ load_out) {
+  extern __shared__ int sm[];
+  int* load = sm;       // [P]
+  int* done = sm + P;   // [E]
+  if (threadIdx.x != 0) return;
+  const int per = E / P;
+  long long R = 0;
+  for (int e = 0; e < E; ++e) R += counts[e];
+  const int C = static_cast<int>((R + P - 1) / P);
+  int n = 0;
+  for (int r = 0; r < P; ++r) {
+    load[r] = 0;
+    for (int e = r * per; e < (r + 1) * per; ++e) {
+      const int take = min(counts[e], C - load[r]);
+      done[e] = 0;
+      if (take > 0) {
+        pieces[4 * n] = e; pieces[4 * n + 1] = r; pieces[4 * n + 2] = 0; pieces[4 * n + 3] = take;
+        ++n;
+        load[r] += take;
+        done[e] = take;
+      }
+    }
+  }
+  for (int e = 0; e < E; ++e) {
+    int r = 0;
+    while (done[e] < counts[e]) {
+      while (load[r] >= C) ++r;
+      const int take = min(counts[e] - done[e], C - load[r]);
+      pieces[4 * n] = e; pieces[4 * n + 1] = r; pieces[4 * n + 2] = done[e]; pieces[4 * n + 3] = take;
+      ++n;
+      load[r] += take;
+      done[e] += take;
+    }
+  }
+  *n_pieces = n;
+  for (int r = 0; r < P; ++r) load_out[r] = load[r];
+}
+
+}  // namespace
+
+cudaError_t launch_replica_plan(const int* counts, int E, int P, int* pieces, int* n_pieces,
+                                int* load, cudaStream_t st) {
+  LaunchTimer lt("replica_plan", st);
+  replica_plan_kernel<<<1, 32, static_cast<size_t>(E + P) * sizeof(int), st>>>(counts, E, P, pieces,
+                                                                                n_pieces, load);
   return cudaGetLastError();
 }
 

@@ -28,9 +28,10 @@ BF16 = torch.bfloat16
 
 class LatentMoELayer:
     def __init__(self, weights: dict, T: int, k: int, wgrad_dtype: int = M.MOE_DTYPE_F32,
-                 device="cuda", fused_gather: bool = False):
+                 device="cuda", fused_gather: bool = False, aux_scale: float = 0.0):
         self.w = weights
         self.fused_gather = fused_gather
+        self.aux_scale = aux_scale  # > 0: add aux_scale * the auxiliary balance loss
         self.T = T
         self.k = k
         self.d, self.E = weights["Wr"].shape
@@ -86,7 +87,10 @@ class LatentMoELayer:
             "gbwd": ws(M.MOE_OP_GROUPED_SWIGLU_BWD, T=R, k=1, f=f),
             "sbwd": ws(M.MOE_OP_SHARED_SWIGLU_BWD, T=T_, l=l, f=f, S=S),
             "rbwd": ws(M.MOE_OP_ROUTE_TOPK_BWD, T=T_, E=E),
+            "aux": ws(M.MOE_OP_ROUTER_AUX, T=T_, E=E),
         }
+        self.p_mean = e(E, dt=torch.float32)
+        self.aux_loss = e(1, dt=torch.float32)
         self.ws = {n: torch.empty(max(b, 256), dtype=torch.uint8, device=dev)
                    for n, b in self.ws_sizes.items()}
 
@@ -97,6 +101,10 @@ class LatentMoELayer:
         self.x = x
         M.moe_route_topk(x, w["Wr"], w.get("bias"), T, d, E, k, self.topk_idx, self.topk_w,
                          self.topk_s, self.ws["route"], self.ws_sizes["route"], self.err, stream)
+        if self.aux_scale > 0:
+            # the router logits stay in the route workspace until the backward
+            M.moe_router_aux_loss(self.ws["route"], w.get("bias"), T, E, self.p_mean, self.aux_loss,
+                                  self.ws["aux"], self.ws_sizes["aux"], stream)
         M.moe_latent_proj(x, w["W_dn"], T, d, l, self.z, stream)
         fused = self.fused_gather
         M.moe_permute(None if fused else self.z, self.topk_idx, self.topk_w, T, l, E, k,
@@ -141,9 +149,12 @@ class LatentMoELayer:
                                 self.ws["sbwd"], self.ws_sizes["sbwd"], stream)
         M.moe_permute_bwd(self.dz_perm, self.slot_of, self.dz_sh, T, k, l, self.dz, stream)
         M.moe_latent_proj_bwd(self.dz, self.x, w["W_dn"], T, d, l, self.dx, g["W_dn"], wd, stream)
+        aux = self.aux_scale > 0
         M.moe_route_topk_bwd(self.d_row_w, self.slot_of, self.topk_idx, self.topk_w, self.topk_s,
                              self.x, w["Wr"], T, d, E, k, self.d_topk_w, self.dx, g["Wr"], wd,
-                             self.ws["rbwd"], self.ws_sizes["rbwd"], self.err, stream)
+                             self.ws["route"] if aux else None, w.get("bias") if aux else None,
+                             self.p_mean if aux else None, self.aux_scale, self.ws["rbwd"],
+                             self.ws_sizes["rbwd"], self.err, stream)
         return self.dx
 
     def step(self, x, dout, stream=None):

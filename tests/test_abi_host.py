@@ -51,6 +51,7 @@ def test_workspace_sizes(lib):
     assert M.moe_workspace_size(M.MOE_OP_GROUPED_SWIGLU_BWD, T=100, k=1, f=64) >= \
         100 * (2 * 64 * 2 + 64 * 2 + 4)
     assert M.moe_workspace_size(M.MOE_OP_ROUTE_TOPK_BWD, T=10, E=64) >= 10 * 64 * 2
+    assert M.moe_workspace_size(M.MOE_OP_ROUTER_AUX, T=4096, E=896) >= 256 * 896 * 4
 
 
 def test_argument_errors_before_any_cuda_call(lib):

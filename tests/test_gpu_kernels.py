@@ -314,7 +314,7 @@ def test_route_topk_bwd():
     M.moe_route_topk_bwd(dev(d_row_w), dev(torch.from_numpy(slot_of).int()),
                          dev(torch.from_numpy(idx).int()), dev(torch.from_numpy(w).float()),
                          dev(torch.from_numpy(s).float()), dev(x), dev(Wr), T, d, E, k, d_topk_w,
-                         dx_d, dWr, M.MOE_DTYPE_F32, ws, wsb)
+                         dx_d, dWr, M.MOE_DTYPE_F32, None, None, None, 0.0, ws, wsb)
     torch.cuda.synchronize()
     dw = f64(d_row_w)[slot_of]
     np.testing.assert_array_equal(d_topk_w.cpu().numpy(), d_row_w.numpy()[slot_of])
@@ -378,3 +378,57 @@ def test_gather_fused_grouped_gemms_equal_explicit_permute(T, E, k, l, f, skew):
     for name, a, b in zip(("gu", "h", "y", "dz", "d_row_w", "dW13", "dW2"), *outs):
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b), name
+
+
+@pytest.mark.parametrize("T,E,bias", [(333, 64, False), (4096, 896, True), (1, 64, False)])
+def test_router_aux_loss_and_gradient(T, E, bias):
+    L = I.make_logits(60 + T, T, E)
+    b = (torch.randn(E, generator=torch.Generator().manual_seed(6)) * 0.5).float() if bias else None
+    p_mean = torch.empty(E, dtype=torch.float32, device="cuda")
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    wsb = M.moe_workspace_size(M.MOE_OP_ROUTER_AUX, T=T, E=E)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    Ld, bd = dev(L), (dev(b) if bias else None)
+    M.moe_router_aux_loss(Ld, bd, T, E, p_mean, loss, ws, wsb)
+    torch.cuda.synchronize()
+    ref_p, ref_loss = O.aux_balance_loss(L.numpy(), b.numpy() if bias else None)
+    np.testing.assert_allclose(p_mean.cpu().numpy(), ref_p, rtol=2e-5, atol=1e-9)
+    assert abs(loss.item() - ref_loss) < 2e-5 * abs(ref_loss)
+    # gradient through moe_route_topk_bwd: zero routing-weight gradient, so dL is the aux term
+    k = 4
+    idx = O.topk_select(L.numpy() + (b.numpy()[None, :] if bias else 0), k)
+    slot_of, _, _ = O.permutation_maps(idx, E)
+    d = 128
+    x = _bf16(61, T, d)
+    Wr = _bf16(62, d, E, std=0.02)
+    dWr = torch.empty(d, E, dtype=torch.float32, device="cuda")
+    wsb2 = M.moe_workspace_size(M.MOE_OP_ROUTE_TOPK_BWD, T=T, E=E)
+    ws2 = torch.empty(wsb2, dtype=torch.uint8, device="cuda")
+    ones = torch.full((T, k), 0.25, dtype=torch.float32)
+    M.moe_route_topk_bwd(dev(torch.zeros(T * k)), dev(torch.from_numpy(slot_of).int()),
+                         dev(torch.from_numpy(idx).int()), dev(ones), dev(ones), dev(x), dev(Wr), T,
+                         d, E, k, None, None, dWr, M.MOE_DTYPE_F32, Ld, bd, p_mean, 3.0, ws2, wsb2)
+    torch.cuda.synchronize()
+    dL = O.aux_balance_loss_backward(L.numpy(), b.numpy() if bias else None, scale=3.0)
+    check_close("dWr_aux", f64(dWr), f64(x).T @ dL, scale_by_max=True)
+
+
+@pytest.mark.parametrize("case", ["page", "zipf", "ep"])
+def test_replica_plan_bit_exact(case):
+    if case == "page":
+        counts, P = np.array([12, 1, 2, 9, 0, 3, 4, 1]), 8
+    elif case == "zipf":
+        idx = I.make_topk_ids(70, 4096, 896, 16, skew=1.1).numpy()
+        counts, P = O.expert_counts(idx, 896), 64
+    else:
+        counts, P = I.make_ep_rank_inputs()["counts"].numpy(), 14
+    E = len(counts)
+    pieces = torch.full(((2 * E + P), 4), -1, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    load = torch.empty(P, dtype=torch.int32, device="cuda")
+    M.moe_replica_plan(dev(torch.from_numpy(np.asarray(counts)).int()), E, P, pieces, n, load)
+    torch.cuda.synchronize()
+    ref_pieces, ref_load = O.replica_plan(counts, P)
+    assert int(n.item()) == len(ref_pieces)
+    assert pieces[: len(ref_pieces)].cpu().tolist() == [list(p) for p in ref_pieces]
+    assert load.cpu().tolist() == ref_load

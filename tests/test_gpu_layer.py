@@ -207,3 +207,23 @@ def test_layer_fwd_bwd_T16384_sampled():
                 scale_by_max=True)
     check_close("dW_dn", f64(layer.grads["W_dn"]), f64(inp["x"]).T @ f64(layer.dz),
                 scale_by_max=True)
+
+
+def test_layer_cfg0_with_aux_balance_loss():
+    """aux_scale * (negative routing entropy) added to the loss: the aux loss and
+    the router's gradients (dx, dWr) against the oracle with the aux term."""
+    inp = I.make_layer_inputs(0)
+    cfg = inp["cfg"]
+    layer = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32, aux_scale=0.5)
+    layer.forward(inp["x"].cuda())
+    layer.backward(inp["g"].cuda())
+    torch.cuda.synchronize()
+    fwd = O.layer_forward(inp)
+    bwd = O.layer_backward(inp, fwd)
+    p_ref, loss_ref = O.aux_balance_loss(fwd["L"])
+    np.testing.assert_allclose(layer.p_mean.cpu().numpy(), p_ref, rtol=1e-4)
+    assert abs(layer.aux_loss.item() - loss_ref) < 1e-4 * abs(loss_ref)
+    dL_aux = O.aux_balance_loss_backward(fwd["L"], None, scale=0.5)
+    x = f64(inp["x"])
+    check_close("dx", f64(layer.dx), bwd["dx"] + dL_aux @ f64(inp["Wr"]).T)
+    check_close("dWr", f64(layer.grads["Wr"]), bwd["dWr"] + x.T @ dL_aux, scale_by_max=True)

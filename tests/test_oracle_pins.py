@@ -345,3 +345,85 @@ def test_zipf_workload_statistics():
     top = np.sort(counts)[::-1]
     assert top[:45].sum() / counts.sum() > 0.30
     assert 150 <= int((counts <= 2).sum()) <= 260
+
+
+# ---------------------------------------------------------------- auxiliary balance loss
+
+def test_aux_loss_balanced_closed_form():
+    """Equal logits: every token spreads evenly, pbar = 1/E, loss = -log E and
+    the gradient vanishes (the balanced point is the loss's minimum)."""
+    L = np.full((7, 12), 0.3)
+    pbar, loss = O.aux_balance_loss(L)
+    np.testing.assert_allclose(pbar, 1.0 / 12, rtol=1e-15)
+    assert abs(loss + math.log(12.0)) < 1e-14
+    np.testing.assert_allclose(O.aux_balance_loss_backward(L), 0.0, atol=1e-17)
+
+
+def test_aux_loss_two_experts_by_hand():
+    """Two tokens, two experts, logits (ln3, 0) and (0, 0): s = (3/4, 1/2) and
+    (1/2, 1/2), P = (3/5, 2/5) and (1/2, 1/2), pbar = (11/20, 9/20)."""
+    L = np.array([[math.log(3.0), 0.0], [0.0, 0.0]])
+    pbar, loss = O.aux_balance_loss(L)
+    np.testing.assert_allclose(pbar, [0.55, 0.45], rtol=1e-14)
+    assert abs(loss - (0.55 * math.log(0.55) + 0.45 * math.log(0.45))) < 1e-14
+    # skewed experts: raising expert 0's logit on any token makes it worse
+    g = O.aux_balance_loss_backward(L)
+    assert g[0, 0] > 0 and g[1, 0] > 0 and g[0, 1] < 0 and g[1, 1] < 0
+
+
+def test_aux_loss_gradient_finite_differences():
+    rng = np.random.default_rng(12)
+    L = rng.standard_normal((9, 7)) * 1.3
+    b = rng.standard_normal(7) * 0.2
+    g = O.aux_balance_loss_backward(L, b, scale=0.7)
+    h = 1e-6
+    for (t, e) in [(0, 0), (3, 5), (8, 2), (4, 6)]:
+        Lp, Lm = L.copy(), L.copy()
+        Lp[t, e] += h
+        Lm[t, e] -= h
+        fd = 0.7 * (O.aux_balance_loss(Lp, b)[1] - O.aux_balance_loss(Lm, b)[1]) / (2 * h)
+        assert abs(fd - g[t, e]) < 1e-8 * max(1.0, abs(fd)), (t, e, fd, g[t, e])
+
+
+# ---------------------------------------------------------------- replica planner
+
+def _check_plan(counts, P, pieces, load):
+    E = len(counts)
+    C = -(-sum(counts) // P)
+    assert sum(load) == sum(counts) and max(load) <= C
+    # every expert's rows are covered exactly once, in contiguous pieces
+    for e in range(E):
+        mine = sorted((p for p in pieces if p[0] == e), key=lambda p: p[2])
+        pos = 0
+        for (_, _, first, n) in mine:
+            assert first == pos and n > 0
+            pos += n
+        assert pos == counts[e]
+    per = E // P
+    # an expert's first piece stays on its owning rank whenever that rank had room
+    for (e, r, first, n) in pieces:
+        if first == 0 and n > 0 and r != e // per:
+            owner = e // per
+            assert load[owner] == C
+    for r in range(P):
+        assert load[r] == sum(p[3] for p in pieces if p[1] == r)
+
+
+def test_replica_plan_page_illustration():
+    """32 tasks spread unevenly over 8 ranks (one expert per rank) end as 4 per rank."""
+    counts = [12, 1, 2, 9, 0, 3, 4, 1]
+    pieces, load = O.replica_plan(counts, 8)
+    assert load == [4] * 8
+    _check_plan(counts, 8, pieces, load)
+    # the hot experts 0 and 3 get replicas, expert identity is kept
+    assert {p[0] for p in pieces if p[1] != p[0]} == {0, 3}
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_replica_plan_invariants(seed):
+    rng = np.random.default_rng(seed)
+    P = int(rng.choice([1, 2, 4, 8]))
+    E = P * int(rng.integers(1, 6))
+    counts = rng.multinomial(int(rng.integers(0, 400)), rng.dirichlet(np.full(E, 0.3))).tolist()
+    pieces, load = O.replica_plan(counts, P)
+    _check_plan(counts, P, pieces, load)
