@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the secondary workloads (T=4096 forward uniform / Zipf, EP rank)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling case: override T (the JSON line then names that case)")
     ap.add_argument("--experts", type=int, default=0,
@@ -256,6 +258,98 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU arm
 
+def _event_time(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def secondary_workloads(steps, warmup, tc_peak):
+    """Forward-only tokens/s at T=4096 (uniform and Zipf-skewed routing) and the
+    expert-parallel rank workload (grouped SwiGLU GEMMs + return to arrival
+    order, 14 experts x 65536 rows), each timed with CUDA events after warm-up.
+    Returns a dict for the JSON line."""
+    import numpy as np
+    import torch
+
+    from sparse_moe_layer_topk_gb300 import _lib as M
+    from sparse_moe_layer_topk_gb300 import inputs as I
+    from sparse_moe_layer_topk_gb300.layer import LatentMoELayer, weights_to_device
+    out = {}
+    stream = torch.cuda.current_stream()
+    for cid in (1, 2):
+        cfg = I.CONFIGS[cid]
+        inp = I.make_layer_inputs(cfg)
+        layer = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32)
+        x = inp["x"].cuda()
+        ms = _event_time(lambda: layer.forward(x), steps, warmup, stream)
+        counts = layer.counts.cpu().numpy()
+        out[cfg.name] = {"forward_ms": round(ms, 4), "tokens_per_s": cfg.T / (ms / 1000.0),
+                         "experts_with_0_to_2_rows": int((counts <= 2).sum())}
+        # grouped experts alone: natural expert order vs bucketed order (big experts first)
+        w_ = layer.w
+        E, R, l, f = cfg.E, layer.R, cfg.l, cfg.f
+        order = torch.empty(E, dtype=torch.int32, device="cuda")
+        sched_o = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        M.moe_expert_buckets(layer.counts, E, order, sched_o)
+
+        def natural():
+            M.moe_grouped_swiglu(layer.z_perm, w_["W13"], w_["W2"], layer.offsets,
+                                 layer.tile_sched, layer.row_w, E, R, l, f, layer.gu, layer.h,
+                                 layer.y_perm)
+
+        def bucketed():
+            M.moe_grouped_swiglu_ordered(layer.z_perm, w_["W13"], w_["W2"], layer.offsets, sched_o,
+                                         order, layer.row_w, E, R, l, f, layer.gu, layer.h,
+                                         layer.y_perm)
+        out[cfg.name]["grouped_swiglu_ms"] = round(_event_time(natural, steps, warmup, stream), 4)
+        out[cfg.name]["grouped_swiglu_bucketed_ms"] = round(
+            _event_time(bucketed, steps, warmup, stream), 4)
+        del layer, inp, x
+        torch.cuda.empty_cache()
+    ep = I.make_ep_rank_inputs()
+    c = ep["cfg"]
+    counts = ep["counts"].numpy().astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    sched = np.concatenate([[0], np.cumsum((counts + 127) // 128)]).astype(np.int32)
+    z, W13, W2, w = (ep["z_perm"].cuda(), ep["W13"].cuda(), ep["W2"].cuda(), ep["w"].cuda())
+    off, sch = torch.from_numpy(offsets).cuda(), torch.from_numpy(sched).cuda()
+    perm = ep["perm"].numpy()
+    inv = np.empty(c.R, dtype=np.int32)
+    inv[perm] = np.arange(c.R, dtype=np.int32)
+    slot = torch.from_numpy(inv).reshape(c.R, 1).cuda()
+    h = torch.empty(c.R, c.f, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(c.R, c.l, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty(c.R, c.l, dtype=torch.bfloat16, device="cuda")
+
+    def ep_step():
+        M.moe_grouped_swiglu(z, W13, W2, off, sch, w, c.E, c.R, c.l, c.f, None, h, y)
+        M.moe_unpermute_combine(y, slot, None, c.R, 1, c.l, o)
+
+    M.moe_timing_report()
+    M.moe_timing_enable(True)
+    ms = _event_time(ep_step, steps, warmup, stream)
+    M.moe_timing_enable(False)
+    per = M.moe_timing_report()
+    g_ms = sum(per[n][1] for n in ("expert_gemm1_swiglu", "expert_gemm2_rowscale") if n in per)
+    g_n = per.get("expert_gemm1_swiglu", (1, 0))[0]
+    flops = 2 * c.R * c.l * 2 * c.f + 2 * c.R * c.f * c.l
+    g_avg = g_ms / max(g_n, 1) / 1000.0
+    out[c.name] = {"ms": round(ms, 4), "rows_per_s": c.R / (ms / 1000.0),
+                   "grouped_gemm_tflops": flops / g_avg / 1e12,
+                   "grouped_gemm_pct_bf16_peak": 100.0 * flops / g_avg / 1e12 / tc_peak}
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -391,6 +485,12 @@ def run_ours(args):
     g_ms = sum(per_kernel[n][1] for n in EXPERT_GEMMS if n in per_kernel)
     grouped_pct = 100.0 * (g_fl / (g_ms / 1000.0) / 1e12) / tc if g_ms else None
 
+    secondary = None
+    if rank == 0 and not args.no_secondary and not (args.tokens or args.experts):
+        del layer
+        torch.cuda.empty_cache()
+        secondary = secondary_workloads(20, 3, tc)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         n = args.cpu_sample_tokens
@@ -412,6 +512,7 @@ def run_ours(args):
                              "activations streamed per step); no explicit flush"},
             "roofline": roof,
             "grouped_gemm_pct_bf16_peak": grouped_pct,
+            "secondary": secondary,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,

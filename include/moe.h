@@ -204,6 +204,25 @@ int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16
                        int E, int R, int l, int f, uint16_t* gu_save, uint16_t* h,
                        uint16_t* y_perm, void* stream);
 
+/* Multi-bucket batching ("大模型落地昇腾" page, section "二、算力侧": experts with
+ * similar token counts grouped into buckets, each with one batch shape), read
+ * for this engine as an expert order: bucket class 0 for an empty expert, else
+ * 1 + floor(log2(ceil(count / 128))); experts by class, largest first,
+ * ascending id within a class, empty experts last (expert_order[E]); and
+ * tile_sched_ordered[E+1], the exclusive scan of ceil(count / 128) in that
+ * order. One CTA on the device from moe_permute's counts; E <= 1024. */
+int moe_expert_buckets(const int32_t* counts, int E, int32_t* expert_order,
+                       int32_t* tile_sched_ordered, void* stream);
+
+/* moe_grouped_swiglu walking the experts in a given order (tile_sched_ordered
+ * and expert_order from moe_expert_buckets): the persistent tiles then run
+ * the big experts first. Results are identical to moe_grouped_swiglu. */
+int moe_grouped_swiglu_ordered(const uint16_t* z_perm, const uint16_t* W13, const uint16_t* W2,
+                               const int32_t* offsets, const int32_t* tile_sched_ordered,
+                               const int32_t* expert_order, const float* row_w, int E, int R,
+                               int l, int f, uint16_t* gu_save, uint16_t* h, uint16_t* y_perm,
+                               void* stream);
+
 /* moe_grouped_swiglu with the permute fused into GEMM1's operand load: the
  * permuted rows are never written. z is the unpermuted latent [T][l] and
  * permuted row r is z[token_of[r]] (token_of from moe_permute, which can then

@@ -23,6 +23,8 @@ Sources (the pages give the structure, not the formulas):
           counted from the current routing result.
   [PLAN]  "TorchTitan Ascend开源" page, sections "在线负载规划" and
           "MoonEP动态负载均衡与专家并行优化": online replica planning.
+  [BUCKET] "大模型落地昇腾:从适配挑战到高效训练实践" page, section "二、算力侧":
+          multi-bucket batching of experts with similar token counts.
   [AUX]   "大模型落地昇腾:从适配挑战到高效训练实践" page, section "三、通信侧":
           an auxiliary load-balance loss that constrains the entropy of the
           routing distribution.
@@ -45,7 +47,8 @@ __all__ = [
     "expert_offsets", "permutation_maps", "permute_rows", "swiglu_expert",
     "grouped_swiglu", "combine", "layer_forward", "layer_backward",
     "ep_rank_forward", "m_tiles_schedule", "router_backward", "swiglu_expert_backward",
-    "aux_balance_loss", "aux_balance_loss_backward", "replica_plan",
+    "aux_balance_loss", "aux_balance_loss_backward", "replica_plan", "bucket_order",
+    "expert_bucket_class",
 ]
 
 
@@ -392,6 +395,32 @@ def replica_plan(counts, P: int):
             load[r] += take
             done[e] += take
     return pieces, load
+
+
+# --------------------------------------------------------------------------
+# Multi-bucket batching  [BUCKET]: "大模型落地昇腾" page, section "二、算力侧":
+# experts with similar token counts are grouped into buckets, each run with one
+# batch shape.
+# --------------------------------------------------------------------------
+
+def expert_bucket_class(count, tile_m: int = 128) -> int:
+    """0 for an empty expert, else 1 + floor(log2(ceil(count / tile_m))): experts
+    in one class need the same number of tile_m-row tiles up to a factor < 2."""
+    nt = -(-int(count) // tile_m)
+    return 0 if nt == 0 else 1 + int(nt).bit_length() - 1
+
+
+def bucket_order(counts, tile_m: int = 128):
+    """Experts ordered by bucket class, largest class first, ascending expert id
+    within a class, empty experts last; and the exclusive scan of their row
+    tiles in that order. Returns (order [E], tile_sched_ordered [E+1])."""
+    counts = [int(c) for c in counts]
+    cls = [expert_bucket_class(c, tile_m) for c in counts]
+    order = sorted(range(len(counts)), key=lambda e: (-cls[e], e))
+    sched = [0]
+    for e in order:
+        sched.append(sched[-1] + -(-counts[e] // tile_m))
+    return np.asarray(order, dtype=np.int64), np.asarray(sched, dtype=np.int64)
 
 
 def ep_rank_forward(z_perm, counts, W13, W2, w, perm):

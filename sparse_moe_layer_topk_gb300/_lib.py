@@ -67,6 +67,9 @@ SIGNATURES = {
                             _F, _P, _Z, _P, _P], _I),
     "moe_router_aux_loss": ([_P, _P, _I, _I, _P, _P, _P, _Z, _P], _I),
     "moe_replica_plan": ([_P, _I, _I, _P, _P, _P, _P], _I),
+    "moe_expert_buckets": ([_P, _I, _P, _P, _P], _I),
+    "moe_grouped_swiglu_ordered": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P],
+                                   _I),
     "moe_timing_enable": ([_I], _I),
     "moe_timing_report": ([ctypes.c_char_p, _Z], _I),
 }
@@ -258,3 +261,13 @@ def moe_timing_report() -> dict:
 
 def moe_replica_plan(counts, E, P, pieces, n_pieces, rank_load, stream=None):
     _call("moe_replica_plan", counts, E, P, pieces, n_pieces, rank_load, stream)
+
+
+def moe_expert_buckets(counts, E, expert_order, tile_sched_ordered, stream=None):
+    _call("moe_expert_buckets", counts, E, expert_order, tile_sched_ordered, stream)
+
+
+def moe_grouped_swiglu_ordered(z_perm, W13, W2, offsets, tile_sched_ordered, expert_order, row_w,
+                               E, R, l, f, gu_save, h, y_perm, stream=None):
+    _call("moe_grouped_swiglu_ordered", z_perm, W13, W2, offsets, tile_sched_ordered,
+          expert_order, row_w, E, R, l, f, gu_save, h, y_perm, stream)

@@ -301,7 +301,8 @@ namespace {
 int grouped_swiglu_impl(const uint16_t* z_perm, long long src_rows, const int32_t* gather,
                         const uint16_t* W13, const uint16_t* W2, const int32_t* offsets,
                         const int32_t* tile_sched, const float* row_w, int E, int R, int l, int f,
-                        uint16_t* gu_save, uint16_t* h, uint16_t* y_perm, void* stream) {
+                        uint16_t* gu_save, uint16_t* h, uint16_t* y_perm, void* stream,
+                        const int32_t* expert_order = nullptr) {
   MOE_REQUIRE(z_perm && W13 && W2 && offsets && tile_sched && h && y_perm, MOE_ERR_ARG);
   MOE_REQUIRE(E > 0 && R >= 0 && l > 0 && f > 0, MOE_ERR_ARG);
   MOE_REQUIRE(l % 64 == 0 && f % 64 == 0, MOE_ERR_ALIGN);
@@ -318,6 +319,7 @@ int grouped_swiglu_impl(const uint16_t* z_perm, long long src_rows, const int32_
   L1.G = E;
   L1.offsets = offsets;
   L1.tile_sched = tile_sched;
+  L1.expert_order = expert_order;
   L1.R_cap = R;
   L1.N = f;
   L1.K = l;
@@ -345,6 +347,7 @@ int grouped_swiglu_impl(const uint16_t* z_perm, long long src_rows, const int32_
   L2.G = E;
   L2.offsets = offsets;
   L2.tile_sched = tile_sched;
+  L2.expert_order = expert_order;
   L2.R_cap = R;
   L2.N = l;
   L2.K = f;
@@ -370,6 +373,23 @@ int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16
                        uint16_t* y_perm, void* stream) {
   return grouped_swiglu_impl(z_perm, R, nullptr, W13, W2, offsets, tile_sched, row_w, E, R, l, f,
                              gu_save, h, y_perm, stream);
+}
+
+int moe_expert_buckets(const int32_t* counts, int E, int32_t* expert_order,
+                       int32_t* tile_sched_ordered, void* stream) {
+  MOE_REQUIRE(counts && expert_order && tile_sched_ordered, MOE_ERR_ARG);
+  MOE_REQUIRE(E > 0 && E <= 1024, MOE_ERR_ARG);
+  return cuda_status(launch_bucket_order(counts, E, expert_order, tile_sched_ordered, S(stream)));
+}
+
+int moe_grouped_swiglu_ordered(const uint16_t* z_perm, const uint16_t* W13, const uint16_t* W2,
+                               const int32_t* offsets, const int32_t* tile_sched_ordered,
+                               const int32_t* expert_order, const float* row_w, int E, int R,
+                               int l, int f, uint16_t* gu_save, uint16_t* h, uint16_t* y_perm,
+                               void* stream) {
+  MOE_REQUIRE(expert_order != nullptr, MOE_ERR_ARG);
+  return grouped_swiglu_impl(z_perm, R, nullptr, W13, W2, offsets, tile_sched_ordered, row_w, E, R,
+                             l, f, gu_save, h, y_perm, stream, expert_order);
 }
 
 int moe_grouped_swiglu_gather(const uint16_t* z, const int32_t* token_of, int T,

@@ -45,6 +45,8 @@ struct GemmLaunch {
   int M = 0, N = 0, K = 0, G = 1;
   const int* offsets = nullptr;     // [G+1]
   const int* tile_sched = nullptr;  // [G+1] (SCHED_GROUPED_M)
+  const int* expert_order = nullptr;  // grouped-M: groups walked in this order (tile_sched
+                                      // is then the scan in that order); nullptr = natural
   int R_cap = 0;                    // row capacity (SCHED_GROUPED_M grid bound)
   // operands: A is [M][K] (a_mn = 0) or [K][M] (a_mn = 1);
   //           B is [N][K] (b_mn = 0) or [K][N] (b_mn = 1), optionally batched.

@@ -53,6 +53,7 @@ struct Params {
   int sched, M, N, K, G;
   const int* offsets;
   const int* tile_sched;
+  const int* expert_order;  // grouped-M: position -> group (nullptr: identity)
   int a_mn, b_mn, b_rank3;
   int b_batch_mode, n_tiles_per_batch, k_per_batch;
   int swiglu_b, f;
@@ -107,9 +108,10 @@ __device__ __forceinline__ Tile decode(const Params& p, int t) {
       const int mid = (lo + hi) >> 1;
       if (__ldg(p.tile_sched + mid) * p.nt <= t) lo = mid; else hi = mid;
     }
-    const int g = lo;
-    const int ts0 = __ldg(p.tile_sched + g);
-    const int mtg = __ldg(p.tile_sched + g + 1) - ts0;
+    const int pos = lo;
+    const int g = p.expert_order ? __ldg(p.expert_order + pos) : pos;
+    const int ts0 = __ldg(p.tile_sched + pos);
+    const int mtg = __ldg(p.tile_sched + pos + 1) - ts0;
     const int local = t - ts0 * p.nt;
     ti.g = g;
     ti.n_blk = local / mtg;
@@ -834,6 +836,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   p.G = L.G;
   p.offsets = L.offsets;
   p.tile_sched = L.tile_sched;
+  p.expert_order = L.expert_order;
   p.a_mn = L.a_mn;
   p.b_mn = L.b_mn;
   const bool b3 = L.b_batch_mode != BATCH_NONE || L.B.batch > 1;

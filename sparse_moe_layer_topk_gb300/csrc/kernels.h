@@ -34,4 +34,7 @@ cudaError_t launch_aux_bwd(const float* L, const float* bias, const float* p_mea
 cudaError_t launch_replica_plan(const int* counts, int E, int P, int* pieces, int* n_pieces,
                                 int* load, cudaStream_t st);
 
+cudaError_t launch_bucket_order(const int* counts, int E, int* order, int* sched,
+                                cudaStream_t st);
+
 }  // namespace moe

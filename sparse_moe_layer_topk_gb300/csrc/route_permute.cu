@@ -665,3 +665,56 @@ cudaError_t launch_replica_plan(const int* counts, int E, int P, int* pieces, in
 }
 
 }  // namespace moe
+
+namespace moe {
+namespace {
+
+// Expert order for bucketed batching (one CTA of 1024 threads, E <= 1024):
+// class 0 = empty, else 1 + floor(log2(row tiles)); largest class first,
+// ascending expert id within a class; then the exclusive scan of the row
+// tiles in that order.
+__global__ void __launch_bounds__(1024) bucket_order_kernel(const int* __restrict__ counts, int E,
+                                                           int* __restrict__ order,
+                                                           int* __restrict__ sched) {
+  __shared__ int warp_sums[32];
+  __shared__ int class_n[32];
+  __shared__ int tiles_at[1024];
+  const int e = threadIdx.x;
+  const int nt = e < E ? (counts[e] + 127) >> 7 : 0;
+  const int cls = e < E ? (nt == 0 ? 0 : 32 - __clz(nt)) : -1;  // 1 + floor(log2 nt)
+  if (e < 32) class_n[e] = 0;
+  __syncthreads();
+  if (e < E) atomicAdd(&class_n[cls], 1);
+  __syncthreads();
+  int pos = -1;
+  int base = 0;
+  for (int c = 31; c >= 0; --c) {  // classes in descending order
+    const int n = class_n[c];      // uniform across the block
+    if (n == 0) continue;
+    const int flag = (cls == c) ? 1 : 0;
+    const int rank = block_inclusive_scan(flag, warp_sums, nullptr) - flag;
+    if (flag) pos = base + rank;
+    base += n;
+  }
+  if (e < E) {
+    order[pos] = e;
+    tiles_at[pos] = nt;
+  }
+  __syncthreads();
+  const int v = e < E ? tiles_at[e] : 0;
+  int total = 0;
+  const int incl = block_inclusive_scan(v, warp_sums, &total);
+  if (e < E) sched[e] = incl - v;
+  if (e == 0) sched[E] = total;
+}
+
+}  // namespace
+
+cudaError_t launch_bucket_order(const int* counts, int E, int* order, int* sched,
+                                cudaStream_t st) {
+  LaunchTimer lt("bucket_order", st);
+  bucket_order_kernel<<<1, 1024, 0, st>>>(counts, E, order, sched);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -432,3 +432,36 @@ def test_replica_plan_bit_exact(case):
     assert int(n.item()) == len(ref_pieces)
     assert pieces[: len(ref_pieces)].cpu().tolist() == [list(p) for p in ref_pieces]
     assert load.cpu().tolist() == ref_load
+
+
+@pytest.mark.parametrize("skew", [0.0, 1.1, 2.0])
+def test_bucket_order_and_ordered_grouped_gemm(skew):
+    T, E, k, l, f = 2048, 128, 8, 256, 128
+    idx = I.make_topk_ids(80, T, E, k, skew=skew)
+    z = _bf16(81, T, l)
+    tw = torch.rand(T, k, generator=torch.Generator().manual_seed(8)) * 0.2 + 0.01
+    g = _run_permute(idx, E, l, z, tw)
+    counts = g["counts"].numpy()
+    order = torch.empty(E, dtype=torch.int32, device="cuda")
+    sched_o = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    M.moe_expert_buckets(dev(g["counts"]), E, order, sched_o)
+    torch.cuda.synchronize()
+    ref_order, ref_sched = O.bucket_order(counts)
+    np.testing.assert_array_equal(order.cpu().numpy(), ref_order)
+    np.testing.assert_array_equal(sched_o.cpu().numpy(), ref_sched)
+    R = T * k
+    W13 = dev(_bf16(82, E, l, 2 * f, std=0.02))
+    W2 = dev(_bf16(83, E, f, l, std=0.02))
+    outs = []
+    for ordered in (False, True):
+        h = torch.empty(R, f, dtype=torch.bfloat16, device="cuda")
+        y = torch.empty(R, l, dtype=torch.bfloat16, device="cuda")
+        if ordered:
+            M.moe_grouped_swiglu_ordered(dev(g["z_perm"]), W13, W2, dev(g["offsets"]), sched_o, order,
+                                         dev(g["row_w"]), E, R, l, f, None, h, y)
+        else:
+            M.moe_grouped_swiglu(dev(g["z_perm"]), W13, W2, dev(g["offsets"]), dev(g["tile_sched"]),
+                                 dev(g["row_w"]), E, R, l, f, None, h, y)
+        torch.cuda.synchronize()
+        outs.append((h.cpu().view(torch.int16), y.cpu().view(torch.int16)))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])

@@ -427,3 +427,27 @@ def test_replica_plan_invariants(seed):
     counts = rng.multinomial(int(rng.integers(0, 400)), rng.dirichlet(np.full(E, 0.3))).tolist()
     pieces, load = O.replica_plan(counts, P)
     _check_plan(counts, P, pieces, load)
+
+
+# ---------------------------------------------------------------- bucket order
+
+def test_bucket_classes_by_hand():
+    assert [O.expert_bucket_class(c) for c in (0, 1, 128, 129, 256, 257, 512, 1024, 1025)] == \
+        [0, 1, 1, 2, 2, 2, 3, 4, 4]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bucket_order_invariants(seed):
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(1, 200))
+    counts = rng.multinomial(int(rng.integers(0, 30000)), rng.dirichlet(np.full(E, 0.3)))
+    order, sched = O.bucket_order(counts)
+    assert sorted(order.tolist()) == list(range(E))
+    cls = [O.expert_bucket_class(counts[e]) for e in order]
+    assert all(a >= b for a, b in zip(cls, cls[1:]))
+    for c in set(cls):
+        ids = [e for e in order if O.expert_bucket_class(counts[e]) == c]
+        assert ids == sorted(ids)
+    tiles = [(int(counts[e]) + 127) // 128 for e in order]
+    assert sched.tolist() == [0] + np.cumsum(tiles).tolist()
+    assert sched[-1] == O.m_tiles_schedule(counts)[-1]
