@@ -39,14 +39,18 @@ constexpr int CHUNK_BYTES = 64 * 128;  // one 64-row x 128-byte swizzled block
 
 // BN: tile width (UMMA N); EW: epilogue warps (4, or 8 for heavy epilogues:
 // two warps per TMEM lane quadrant, splitting the tile's column chunks).
-template <int BN, int EW>
+template <int BN, int EW, bool CW16 = false>
 struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? (EW == 8 ? 3 : 4) : (EW == 8 ? 5 : 6);
+  static constexpr int STAGES = (BN == 256) ? ((EW == 8 && !CW16) ? 3 : 4)
+                                            : ((EW == 8 && !CW16) ? 5 : 6);
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int THREADS = 64 + 32 * EW;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * 6144 + 1024 + 1024;
+  // per-warp output staging: 32-column blocks (one 4 KB fp32 block or three 2 KB
+  // bf16 blocks), or three 1 KB 16-column bf16 blocks (CW16: one stage more)
+  static constexpr int STG = CW16 ? 3072 : 6144;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * STG + 1024 + 1024;
 };
 
 struct Params {
@@ -169,13 +173,13 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* err_f
 
 // ------------------------------------------------------------------ producer
 
-template <int BN, int EW, bool WARP>
+template <int BN, int EW, bool CW16, bool WARP>
 __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CUtensorMap* mapB,
                               uint8_t* smem, uint64_t* full, uint64_t* empty, int* sidx,
                               volatile int* abort_flag) {
   // WARP: run by the whole warp (the lanes fetch gather indices and issue the
   // gather4 copies, lane 0 the others); otherwise by lane 0 alone.
-  using C = Cfg<BN, EW>;
+  using C = Cfg<BN, EW, CW16>;
   const uint32_t lane = WARP ? lane_id() : 0u;
   int stage = 0;
   uint32_t phase = 0;
@@ -301,11 +305,11 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
 
 // ------------------------------------------------------------------ MMA
 
-template <int BN, int EW>
+template <int BN, int EW, bool CW16>
 __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                          uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
                          volatile int* abort_flag) {
-  using C = Cfg<BN, EW>;
+  using C = Cfg<BN, EW, CW16>;
   const uint32_t lane = lane_id();
   const uint32_t idesc = make_idesc_bf16(BM, BN, p.a_mn, p.b_mn);
   const uint32_t a_lbo = p.a_mn ? CHUNK_BYTES : 16, b_lbo = p.b_mn ? CHUNK_BYTES : 16;
@@ -393,7 +397,6 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
 // segment (rows past it belong to the next expert) and read-modify-write
 // accumulation.
 
-constexpr int STAGING_PER_WARP = 6144;  // three 2 KB bf16 blocks or one 4 KB fp32 block
 
 __device__ __forceinline__ void store16(void* dst, uint4 v) { *reinterpret_cast<uint4*>(dst) = v; }
 
@@ -417,6 +420,33 @@ __device__ __forceinline__ void stage_f32(uint8_t* blk, int row, const float* v)
     *reinterpret_cast<uint4*>(rp + ((c ^ sw) << 4)) =
         make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
                    __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+}
+
+// Row `row` of a 32x16 bf16 block: 32-byte rows, 32-byte TMA swizzle.
+__device__ __forceinline__ void stage_bf16_16(uint8_t* blk, int row, const float* v) {
+  uint8_t* rp = blk + row * 32;
+  const int sw = (row >> 2) & 1;
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+    *reinterpret_cast<uint4*>(rp + ((c ^ sw) << 4)) =
+        make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                   pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+}
+
+__device__ __forceinline__ void store_bf16_row16(bf16* dst, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+    store16(dst + 8 * c,
+            make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                       pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7])));
+}
+
+__device__ __forceinline__ void ld_chunk16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  tmem_ld_32x32b_x16(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void store_bf16_row(bf16* dst, const float* v) {
@@ -448,7 +478,7 @@ struct StoreMaps {
   int c0_rank3;
 };
 
-template <int BN, int EW>
+template <int BN, int EW, bool CW16>
 __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* staging,
                               uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base,
                               volatile int* abort_flag) {
@@ -458,7 +488,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   const int grp = (warp - 2) / 4;
   const uint32_t lane = lane_id();
   const int r_loc = q * 32 + static_cast<int>(lane);
-  uint8_t* stg = staging + (warp - 2) * STAGING_PER_WARP;
+  uint8_t* stg = staging + (warp - 2) * Cfg<BN, EW, CW16>::STG;
   const uint32_t stg_s = smem_u32(stg);
   const int total = total_tiles(p);
   bool pending = false;  // a bulk store of this warp may still read the staging area
@@ -545,6 +575,46 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           }
         }
       } else if (p.epi == EPI_SWIGLU) {
+        if constexpr (CW16) {
+        // TMEM columns [0, BN/2) hold the gate, [BN/2, BN) the up projection;
+        // 16-column chunks, the two warps of a lane quadrant taking turns.
+        const int out_batch = (p.b_batch_mode == BATCH_FROM_N) ? ti.batch : 0;
+#pragma unroll 1
+        for (int c = grp; c < BN / 32; c += NG) {
+          float g[16], u[16], hv[16];
+          ld_chunk16(trow + c * 16, g);
+          ld_chunk16(trow + BN / 2 + c * 16, u);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hv[i] = g[i] * sigmoidf_(g[i]) * u[i];
+          const int j = ti.nb0 + c * 16;
+          const int hcol = out_batch * p.f + j;
+          const int gcol = out_batch * 2 * p.f + j;
+          if (use_tma) {
+            stage_begin();
+            stage_bf16_16(stg, lane, hv);
+            if (p.gu) {
+              stage_bf16_16(stg + 1024, lane, g);
+              stage_bf16_16(stg + 2048, lane, u);
+            }
+            stage_end();
+            if (lane == 0) {
+              tma_store_2d(sm.c0, stg_s, hcol, row0);
+              if (p.gu) {
+                tma_store_2d(sm.c1, stg_s + 1024, gcol, row0);
+                tma_store_2d(sm.c1, stg_s + 2048, gcol + p.f, row0);
+              }
+              bulk_commit();
+            }
+            pending = true;
+          } else if (row_ok) {
+            store_bf16_row16(p.h + grow * p.ldh + hcol, hv);
+            if (p.gu) {
+              store_bf16_row16(p.gu + grow * p.ldgu + gcol, g);
+              store_bf16_row16(p.gu + grow * p.ldgu + gcol + p.f, u);
+            }
+          }
+        }
+        } else {
         // TMEM columns [0, BN/2) hold the gate, [BN/2, BN) the up projection.
         const int out_batch = (p.b_batch_mode == BATCH_FROM_N) ? ti.batch : 0;
 #pragma unroll 1
@@ -582,6 +652,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             }
           }
         }
+        }
       } else if (p.epi == EPI_ROWSCALE) {
         const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
 #pragma unroll 1
@@ -606,6 +677,99 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           }
         }
       } else {  // EPI_SWIGLU_BWD
+        if constexpr (CW16) {
+        const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
+        float dot = 0.0f;
+        // 16-column chunks; g and u of the warp's next chunk are loaded one chunk
+        // ahead, h of the current chunk at its start (it is needed last).
+        uint4 Gn[2], Un[2];
+        auto load_gu = [&](int n, uint4* G, uint4* U) {
+          const int s = n / p.f;
+          const bf16* gsrc = p.gu + grow * p.ldgu + s * 2 * p.f + (n - s * p.f);
+#pragma unroll
+          for (int vv = 0; vv < 2; ++vv) {
+            G[vv] = *reinterpret_cast<const uint4*>(gsrc + vv * 8);
+            U[vv] = *reinterpret_cast<const uint4*>(gsrc + p.f + vv * 8);
+          }
+        };
+        const uint4 z4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int vv = 0; vv < 2; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
+        if (row_ok && ti.nb0 + grp * 16 < p.N) load_gu(ti.nb0 + grp * 16, Gn, Un);
+        const int sw = (lane >> 2) & 1;  // 32-byte swizzle of this lane's staging row
+#pragma unroll 1
+        for (int c = grp; c < BN / 16; c += NG) {
+          const int n = ti.nb0 + c * 16;  // column of dh within [0, S*f)
+          if (n >= p.N) break;
+          uint4 Gc[2], Uc[2], Hc[2];
+#pragma unroll
+          for (int vv = 0; vv < 2; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; Hc[vv] = z4; }
+          if (row_ok) {
+            const bf16* hsrc = p.h + grow * p.ldh + n;
+#pragma unroll
+            for (int vv = 0; vv < 2; ++vv) Hc[vv] = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
+            if (c + NG < BN / 16 && n + 16 * NG < p.N) load_gu(n + 16 * NG, Gn, Un);
+          }
+          float a[16];
+          ld_chunk16(trow + c * 16, a);
+          const int s = n / p.f;
+          const int jj = n - s * p.f;
+          const int gcol = s * 2 * p.f + jj;
+          if (use_tma) stage_begin();
+          bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + gcol;
+#pragma unroll
+          for (int vv = 0; vv < 2; ++vv) {
+            const uint32_t Gw[4] = {Gc[vv].x, Gc[vv].y, Gc[vv].z, Gc[vv].w};
+            const uint32_t Uw[4] = {Uc[vv].x, Uc[vv].y, Uc[vv].z, Uc[vv].w};
+            const uint32_t Hw[4] = {Hc[vv].x, Hc[vv].y, Hc[vv].z, Hc[vv].w};
+            uint32_t pdg[4], pdu[4], phw[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              float dgv[2], duv[2], hwv[2];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const float av = a[vv * 8 + 2 * e2 + hh];
+                const float gg = hh ? bf16_hi(Gw[e2]) : bf16_lo(Gw[e2]);
+                const float uu = hh ? bf16_hi(Uw[e2]) : bf16_lo(Uw[e2]);
+                const float hv = hh ? bf16_hi(Hw[e2]) : bf16_lo(Hw[e2]);
+                const float sg = sigmoidf_(gg);
+                const float dh = w * av;
+                dgv[hh] = dh * uu * sg * (1.0f + gg * (1.0f - sg));
+                duv[hh] = dh * gg * sg;
+                dot = fmaf(av, hv, dot);
+                hwv[hh] = w * hv;
+              }
+              pdg[e2] = pack_bf16(dgv[0], dgv[1]);
+              pdu[e2] = pack_bf16(duv[0], duv[1]);
+              phw[e2] = pack_bf16(hwv[0], hwv[1]);
+            }
+            const uint4 DG = make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]);
+            const uint4 DU = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
+            const uint4 HW = make_uint4(phw[0], phw[1], phw[2], phw[3]);
+            if (use_tma) {
+              const int off = lane * 32 + ((vv ^ sw) << 4);
+              *reinterpret_cast<uint4*>(stg + off) = DG;
+              *reinterpret_cast<uint4*>(stg + 1024 + off) = DU;
+              if (p.aux) *reinterpret_cast<uint4*>(stg + 2048 + off) = HW;
+            } else if (row_ok) {
+              store16(dgdst + vv * 8, DG);
+              store16(dgdst + p.f + vv * 8, DU);
+              if (p.aux) store16(p.aux + grow * p.ldaux + n + vv * 8, HW);
+            }
+          }
+          if (use_tma) {
+            stage_end();
+            if (lane == 0) {
+              tma_store_2d(sm.c0, stg_s, gcol, row0);
+              tma_store_2d(sm.c0, stg_s + 1024, gcol + p.f, row0);
+              if (p.aux) tma_store_2d(sm.c1, stg_s + 2048, n, row0);
+              bulk_commit();
+            }
+            pending = true;
+          }
+        }
+        if (row_ok && p.dw_part) p.dw_part[grow * p.dw_nparts + ti.n_blk * NG + grp] = dot;
+        } else {
         const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
         float dot = 0.0f;
         // g and u of the next chunk are loaded one chunk ahead, h of the current
@@ -698,6 +862,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           }
         }
         if (row_ok && p.dw_part) p.dw_part[grow * p.dw_nparts + ti.n_blk * NG + grp] = dot;
+        }
       }
     }
     tc_fence_before();
@@ -707,18 +872,18 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   __syncwarp();
 }
 
-template <int BN, int EW>
+template <int BN, int EW, bool CW16>
 __global__ void __launch_bounds__(64 + 32 * EW, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC0,
                    const __grid_constant__ CUtensorMap mapC1, const Params p) {
-  using C = Cfg<BN, EW>;
+  using C = Cfg<BN, EW, CW16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* staging = smem + C::STAGES * C::STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + EW * STAGING_PER_WARP);
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + EW * C::STG);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -755,15 +920,15 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   if (warp == 0) {
     // Gathering launches run the producer on the whole warp (the lanes fetch
     // indices and issue gather4 copies); the others on lane 0 alone.
-    if (p.gather_a || p.gather_b) producer_loop<BN, EW, true>(p, &mapA, &mapB, smem, full, empty,
-                                                              sidx, abort_flag);
-    else if (lane_id() == 0) producer_loop<BN, EW, false>(p, &mapA, &mapB, smem, full, empty,
-                                                          sidx, abort_flag);
+    if (p.gather_a || p.gather_b)
+      producer_loop<BN, EW, CW16, true>(p, &mapA, &mapB, smem, full, empty, sidx, abort_flag);
+    else if (lane_id() == 0)
+      producer_loop<BN, EW, CW16, false>(p, &mapA, &mapB, smem, full, empty, sidx, abort_flag);
   } else if (warp == 1) {
-    mma_loop<BN, EW>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
+    mma_loop<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
   } else {
     const StoreMaps sm{&mapC0, &mapC1, p.c0_rank3};
-    epilogue_loop<BN, EW>(p, sm, staging, tfull, tempty, tmem_base, abort_flag);
+    epilogue_loop<BN, EW, CW16>(p, sm, staging, tfull, tempty, tmem_base, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -810,24 +975,28 @@ bool make_map(CUtensorMap* map, const MatView& v, int box_rows, bool force3d) {
 // TMA stores: bf16 rows of 64 bytes with 64-byte swizzle, fp32 rows of 128 bytes
 // with 128-byte swizzle (the layouts stage_bf16 / stage_f32 write).
 bool make_store_map(CUtensorMap* map, void* ptr, bool f32, bool rank3, long long d0, long long d1,
-                    long long d2, long long ld, long long batch_stride) {
+                    long long d2, long long ld, long long batch_stride, int box_cols = 32) {
   const long long es = f32 ? 4 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1),
                         static_cast<cuuint64_t>(d2)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * es),
                            static_cast<cuuint64_t>(batch_stride * es)};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
+  // the swizzle span equals the staged row: 128 B (fp32 x 32), 64 B (bf16 x 32), 32 B (bf16 x 16)
+  const long long row_bytes = box_cols * es;
+  const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_32B;
   CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         rank3 ? 3 : 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        sw, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int EW>
+template <int BN, int EW, bool CW16>
 int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
-  using C = Cfg<BN, EW>;
+  using C = Cfg<BN, EW, CW16>;
   Params p{};
   p.sched = L.sched;
   p.M = L.M;
@@ -926,12 +1095,13 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
         ok = make_store_map(&mapC0, L.C, f32, false, L.N, rows_out, 1, L.ldc, 0);
       }
     }
-  } else if (L.epi == EPI_SWIGLU) {
-    ok = make_store_map(&mapC0, L.h, false, false, L.ldh, rows_out, 1, L.ldh, 0);
-    if (ok && L.gu) ok = make_store_map(&mapC1, L.gu, false, false, L.ldgu, rows_out, 1, L.ldgu, 0);
+  } else if (L.epi == EPI_SWIGLU) {  // 16-column blocks
+    ok = make_store_map(&mapC0, L.h, false, false, L.ldh, rows_out, 1, L.ldh, 0, 16);
+    if (ok && L.gu)
+      ok = make_store_map(&mapC1, L.gu, false, false, L.ldgu, rows_out, 1, L.ldgu, 0, 16);
   } else if (L.epi == EPI_ROWSCALE) {
     ok = make_store_map(&mapC0, L.C, false, false, L.N, rows_out, 1, L.ldc, 0);
-  } else {  // EPI_SWIGLU_BWD
+  } else {  // EPI_SWIGLU_BWD (32-column blocks)
     ok = make_store_map(&mapC0, L.C, false, false, L.ldc, rows_out, 1, L.ldc, 0);
     if (ok && L.aux)
       ok = make_store_map(&mapC1, L.aux, false, false, L.ldaux, rows_out, 1, L.ldaux, 0);
@@ -942,7 +1112,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EW>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EW, CW16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) {
@@ -954,8 +1124,8 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
   {
     LaunchTimer lt(L.name, stream);
-    gemm_tc_kernel<BN, EW><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mapA, mapB, mapC0, mapC1,
-                                                                          p);
+    gemm_tc_kernel<BN, EW, CW16><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mapA, mapB, mapC0,
+                                                                                mapC1, p);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -1012,10 +1182,18 @@ int gemm_launch(const GemmLaunch& L, cudaStream_t stream) {
   const int ew = gemm_epilogue_warps(L);
   if (L.splitk > 1 && !(L.sched == SCHED_DENSE && L.epi == EPI_STORE && !L.accumulate))
     return MOE_ERR_UNSUPPORTED;
+  // The SwiGLU forward epilogue works on 16-column chunks (smaller staging, one
+  // more pipeline stage); its backward on 32-column chunks.
+  const bool cw16 = L.epi == EPI_SWIGLU;
   int st;
-  if (L.BN == 256) st = ew == 8 ? launch_bn<256, 8>(L, stream) : launch_bn<256, 4>(L, stream);
-  else if (L.BN == 128) st = ew == 8 ? launch_bn<128, 8>(L, stream) : launch_bn<128, 4>(L, stream);
-  else return MOE_ERR_UNSUPPORTED;
+  if (L.BN == 256)
+    st = ew == 4 ? launch_bn<256, 4, false>(L, stream)
+                 : (cw16 ? launch_bn<256, 8, true>(L, stream) : launch_bn<256, 8, false>(L, stream));
+  else if (L.BN == 128)
+    st = ew == 4 ? launch_bn<128, 4, false>(L, stream)
+                 : (cw16 ? launch_bn<128, 8, true>(L, stream) : launch_bn<128, 8, false>(L, stream));
+  else
+    return MOE_ERR_UNSUPPORTED;
   if (st != MOE_OK || L.splitk <= 1) return st;
   const int kslice = ((L.K + L.splitk - 1) / L.splitk + BK - 1) / BK * BK;
   const int nslices = (L.K + kslice - 1) / kslice;

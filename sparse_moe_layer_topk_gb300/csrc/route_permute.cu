@@ -45,7 +45,9 @@ __device__ __forceinline__ unsigned long long sel_key(float v, int e) {
          static_cast<unsigned long long>(~static_cast<uint32_t>(e));
 }
 
-template <int NPL>
+// NPL keys per lane. VEC (E a multiple of 128): lane holds experts
+// 128 i + 4 lane + j, read as float4; otherwise experts lane + 32 i.
+template <int NPL, bool VEC>
 __global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __restrict__ L,
                                                               const float* __restrict__ bias,
                                                               int T, int E, int k,
@@ -59,15 +61,38 @@ __global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __res
   const float* row = L + static_cast<size_t>(t) * E;
   unsigned long long key[NPL];
   bool bad = false;
+  if (VEC) {
+    float4 lv[NPL / 4 > 0 ? NPL / 4 : 1];
 #pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      const float v = __ldg(row + e) + (bias ? __ldg(bias + e) : 0.0f);
-      bad |= !isfinite(v);
-      key[i] = sel_key(v, e);
-    } else {
-      key[i] = 0ull;
+    for (int i = 0; i < NPL / 4; ++i)
+      lv[i] = (128 * i < E) ? __ldg(reinterpret_cast<const float4*>(row + 128 * i) + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < NPL / 4; ++i) {
+      const float vv[4] = {lv[i].x, lv[i].y, lv[i].z, lv[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = 128 * i + 4 * lane + j;
+        if (128 * i < E) {
+          const float v = vv[j] + (bias ? __ldg(bias + e) : 0.0f);
+          bad |= !isfinite(v);
+          key[4 * i + j] = sel_key(v, e);
+        } else {
+          key[4 * i + j] = 0ull;
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        const float v = __ldg(row + e) + (bias ? __ldg(bias + e) : 0.0f);
+        bad |= !isfinite(v);
+        key[i] = sel_key(v, e);
+      } else {
+        key[i] = 0ull;
+      }
     }
   }
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_flag(err_flag, MOE_FLAG_NONFINITE);
@@ -483,12 +508,23 @@ cudaError_t launch_topk(const float* L, const float* bias, int T, int E, int k, 
   const int grid = (T + 7) / 8;
   const int npl = (E + 31) / 32;
   LaunchTimer lt("topk_sigmoid", st);
-  if (npl <= 2) topk_sigmoid_kernel<2><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
-  else if (npl <= 4) topk_sigmoid_kernel<4><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
-  else if (npl <= 8) topk_sigmoid_kernel<8><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
-  else if (npl <= 16) topk_sigmoid_kernel<16><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
-  else if (npl <= 28) topk_sigmoid_kernel<28><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
-  else topk_sigmoid_kernel<32><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag);
+  const bool vec = (E % 128) == 0 && (reinterpret_cast<uintptr_t>(L) & 15u) == 0;
+#define MOE_TOPK(N, V) topk_sigmoid_kernel<N, V><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag)
+  if (vec) {
+    if (npl <= 4) MOE_TOPK(4, true);
+    else if (npl <= 8) MOE_TOPK(8, true);
+    else if (npl <= 16) MOE_TOPK(16, true);
+    else if (npl <= 28) MOE_TOPK(28, true);
+    else MOE_TOPK(32, true);
+  } else {
+    if (npl <= 2) MOE_TOPK(2, false);
+    else if (npl <= 4) MOE_TOPK(4, false);
+    else if (npl <= 8) MOE_TOPK(8, false);
+    else if (npl <= 16) MOE_TOPK(16, false);
+    else if (npl <= 28) MOE_TOPK(28, false);
+    else MOE_TOPK(32, false);
+  }
+#undef MOE_TOPK
   return cudaGetLastError();
 }
 
