@@ -161,6 +161,64 @@ class LatentMoELayer:
         self.forward(x, stream)
         return self.backward(dout, stream)
 
+    def steps_from_host(self, x_host, g_host, dx_host):
+        """Forward + backward for each (x, dout) pair of pinned host tensors,
+        writing each step's input gradient back to the pinned dx_host[i].
+
+        The host->device copy of step i+1 and the device->host copy of step i-1
+        run on their own streams (separate copy engines) while step i computes;
+        device inputs and input gradients are double-buffered and ordered with
+        events, so every step still copies its own inputs in and its gradient
+        out. Returns after the last copy has been enqueued; synchronise the
+        current stream's device to wait for the results."""
+        n = len(x_host)
+        assert len(g_host) == n and len(dx_host) == n
+        dev = self.dx.device
+        comp = torch.cuda.current_stream()
+        h2d = torch.cuda.Stream(device=dev)
+        d2h = torch.cuda.Stream(device=dev)
+        if not hasattr(self, "_pipe"):
+            self._pipe = {
+                "x": [torch.empty_like(self.dx) for _ in range(2)],
+                "g": [torch.empty_like(self.dx) for _ in range(2)],
+                "dx": [torch.empty_like(self.dx) for _ in range(2)],
+            }
+        P = self._pipe
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        loaded = [None] * n
+        computed = [None] * n
+        drained = [None] * n
+
+        def load(i):
+            s = i & 1
+            with torch.cuda.stream(h2d):
+                if i >= 2:
+                    h2d.wait_event(computed[i - 2])  # slot s no longer read by step i-2
+                P["x"][s].copy_(x_host[i], non_blocking=True)
+                P["g"][s].copy_(g_host[i], non_blocking=True)
+                loaded[i] = ev()
+                loaded[i].record(h2d)
+
+        load(0)
+        for i in range(n):
+            s = i & 1
+            if i + 1 < n:
+                load(i + 1)
+            comp.wait_event(loaded[i])
+            if i >= 2:
+                comp.wait_event(drained[i - 2])  # dx slot s copied out by step i-2
+            self.forward(P["x"][s])
+            self.dx = P["dx"][s]  # the backward writes the input gradient into slot s
+            self.backward(P["g"][s])
+            computed[i] = ev()
+            computed[i].record(comp)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(computed[i])
+                dx_host[i].copy_(P["dx"][s], non_blocking=True)
+                drained[i] = ev()
+                drained[i].record(d2h)
+        comp.wait_event(drained[n - 1])
+
 
 def weights_to_device(inp: dict, device="cuda") -> dict:
     names = ("Wr", "W_dn", "W13", "W2", "W13_sh", "W2_sh", "W_up")

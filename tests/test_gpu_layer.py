@@ -227,3 +227,22 @@ def test_layer_cfg0_with_aux_balance_loss():
     x = f64(inp["x"])
     check_close("dx", f64(layer.dx), bwd["dx"] + dL_aux @ f64(inp["Wr"]).T)
     check_close("dWr", f64(layer.grads["Wr"]), bwd["dWr"] + x.T @ dL_aux, scale_by_max=True)
+
+
+def test_steps_from_host_pipeline_matches_step():
+    """The pipelined host-driven steps (copies on their own streams, double-
+    buffered device inputs) give the same input gradients as plain steps."""
+    inp = I.make_layer_inputs(0)
+    cfg = inp["cfg"]
+    layer = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32)
+    g0 = torch.Generator().manual_seed(9)
+    xs = [torch.randn(cfg.T, cfg.d, generator=g0).to(torch.bfloat16).pin_memory() for _ in range(3)]
+    gs = [torch.randn(cfg.T, cfg.d, generator=g0).to(torch.bfloat16).pin_memory() for _ in range(3)]
+    outs = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    layer.steps_from_host(xs, gs, outs)
+    torch.cuda.synchronize()
+    ref = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32)
+    for i in range(3):
+        dx = ref.step(xs[i].cuda(), gs[i].cuda())
+        torch.cuda.synchronize()
+        assert torch.equal(dx.cpu(), outs[i]), i
