@@ -26,13 +26,14 @@ def _bf16(seed, *shape, std=1.0):
 
 # ---------------------------------------------------------------- GEMM engine
 
-@pytest.mark.parametrize("M_,K,N", [(300, 256, 192), (128, 64, 64), (1000, 512, 1024), (5, 128, 256)])
+@pytest.mark.parametrize("M_,K,N", [(300, 256, 192), (128, 64, 64), (1000, 512, 1024), (5, 128, 256),
+                                    (700, 1024, 512), (2000, 1024, 768)])
 def test_latent_proj_and_bwd(M_, K, N):
     """Every operand layout of the tcgen05 engine: A K-major / B MN-major
     (forward), B K-major (dgrad), A and B MN-major (wgrad); ragged M and an
     N tail narrower than the tile."""
     x = _bf16(1, M_, K)
-    W = _bf16(2, K, N, std=0.05)
+    W = _bf16(2, K, N, std=0.02)  # |out| ~ 1: bf16 output rounding stays below 2e-2
     dout = _bf16(3, M_, N)
     out = torch.empty(M_, N, dtype=torch.bfloat16, device="cuda")
     M.moe_latent_proj(dev(x), dev(W), M_, K, N, out)
