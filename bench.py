@@ -233,8 +233,10 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "unit": "tokens/s", "higher_is_better": True}
     if rank != 0:
         return
-    inp = I.make_layer_inputs(cfg, T=args.cpu_sample_tokens)
-    n = args.cpu_sample_tokens
+    # bounded sample: at most ~1024 oracle tokens over the whole run (a few minutes
+    # of fp64 host work), at least 4 per step
+    n = max(4, min(args.cpu_sample_tokens, 1024 // max(1, args.steps + args.warmup)))
+    inp = I.make_layer_inputs(cfg, T=n)
     for _ in range(args.warmup):
         oracle_sample_time(inp, n)
     times = [oracle_sample_time(inp, n) for _ in range(args.steps)]
