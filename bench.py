@@ -107,6 +107,8 @@ def kernel_work(cfg, T):
         "routing_weight_grad_reduce": (0, R * 8 + R * 4),
         "router_bwd_dlogits": (0, T * k * 16 + T * E * b),
         "router_dgrad": (2 * T * E * d, T * E * b + d * E * b + 2 * T * d * b),
+        "down_proj_router_dgrad": (2 * T * d * (l + E),
+                                   T * (l + E) * b + d * (l + E) * b + T * d * b),
         "router_wgrad": (2 * T * d * E, T * d * b + T * E * b + d * E * 4),
     }
 

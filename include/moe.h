@@ -319,7 +319,9 @@ int moe_permute_bwd(const uint16_t* dz_perm, const int32_t* slot_of, const uint1
  *   auxiliary balance loss (moe_router_aux_loss on aux_logits + aux_bias, whose
  *   p_mean is aux_p_mean): dense over all E experts,
  *   dL[t][e] += aux_scale s(1-s) / (T S_t) (ln p_mean[e] - sum_e' P(e'|t) ln p_mean[e'])
- *   dx_accum[T][d] += dL @ Wr^T  (bf16, read-modify-write)
+ *   dx_accum[T][d] += dL @ Wr^T  (bf16, read-modify-write), or, when dz is given,
+ *   dx_accum = dz @ W_dn^T + dL @ Wr^T (overwrite; one GEMM over K = l + E that
+ *   fuses the down-projection's input gradient: dz [T][l], W_dn [d][l])
  *   dWr[d][E] = x^T @ dL         (fp32 or bf16)
  * E must be a multiple of 64. Workspace (dL in bf16):
  * moe_workspace_size(MOE_OP_ROUTE_TOPK_BWD, T, 0, 0, E, 0, 0, 0). */
@@ -327,7 +329,8 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
                        const float* topk_w, const float* topk_s, const uint16_t* x,
                        const uint16_t* Wr, int T, int d, int E, int k, float* d_topk_w,
                        uint16_t* dx_accum, void* dWr, int wgrad_dtype, const float* aux_logits,
-                       const float* aux_bias, const float* aux_p_mean, float aux_scale, void* ws,
+                       const float* aux_bias, const float* aux_p_mean, float aux_scale,
+                       const uint16_t* dz, const uint16_t* W_dn, int l, void* ws,
                        size_t ws_bytes, int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------- diagnostics */

@@ -64,7 +64,7 @@ SIGNATURES = {
                               _I),
     "moe_permute_bwd": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_route_topk_bwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P,
-                            _F, _P, _Z, _P, _P], _I),
+                            _F, _P, _P, _I, _P, _Z, _P, _P], _I),
     "moe_router_aux_loss": ([_P, _P, _I, _I, _P, _P, _P, _Z, _P], _I),
     "moe_replica_plan": ([_P, _I, _I, _P, _P, _P, _P], _I),
     "moe_expert_buckets": ([_P, _I, _P, _P, _P], _I),
@@ -231,11 +231,11 @@ def moe_permute_bwd(dz_perm, slot_of, dz_shared, T, k, l, dz, stream=None):
 
 
 def moe_route_topk_bwd(d_row_w, slot_of, topk_idx, topk_w, topk_s, x, Wr, T, d, E, k, d_topk_w,
-                       dx_accum, dWr, wgrad_dtype, aux_logits, aux_bias, aux_p_mean, aux_scale, ws,
-                       ws_bytes, err_flag=None, stream=None):
+                       dx_accum, dWr, wgrad_dtype, aux_logits, aux_bias, aux_p_mean, aux_scale, dz,
+                       W_dn, l, ws, ws_bytes, err_flag=None, stream=None):
     _call("moe_route_topk_bwd", d_row_w, slot_of, topk_idx, topk_w, topk_s, x, Wr, T, d, E, k,
           d_topk_w, dx_accum, dWr, wgrad_dtype, aux_logits, aux_bias, aux_p_mean, float(aux_scale),
-          ws, ws_bytes, err_flag, stream)
+          dz, W_dn, l, ws, ws_bytes, err_flag, stream)
 
 
 def moe_router_aux_loss(logits, bias, T, E, p_mean, loss, ws, ws_bytes, stream=None):

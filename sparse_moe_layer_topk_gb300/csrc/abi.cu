@@ -743,7 +743,8 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
                        const float* topk_w, const float* topk_s, const uint16_t* x,
                        const uint16_t* Wr, int T, int d, int E, int k, float* d_topk_w,
                        uint16_t* dx_accum, void* dWr, int wgrad_dtype, const float* aux_logits,
-                       const float* aux_bias, const float* aux_p_mean, float aux_scale, void* ws,
+                       const float* aux_bias, const float* aux_p_mean, float aux_scale,
+                       const uint16_t* dz, const uint16_t* W_dn, int l, void* ws,
                        size_t ws_bytes, int32_t* err_flag, void* stream) {
   MOE_REQUIRE(d_row_w && slot_of && topk_idx && topk_w && topk_s, MOE_ERR_ARG);
   MOE_REQUIRE(T >= 0 && d > 0 && E > 0 && E <= 1024 && k >= 1 && k <= 32 && k <= E, MOE_ERR_ARG);
@@ -768,7 +769,30 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
     MOE_REQUIRE(aux_p_mean != nullptr, MOE_ERR_ARG);
     MOE_CHECK(cuda_status(launch_aux_bwd(aux_logits, aux_bias, aux_p_mean, T, E, aux_scale, dL, st)));
   }
-  if (dx_accum) MOE_CHECK(dense_gemm("router_dgrad", dL, E, 0, Wr, E, 0, T, d, E, dx_accum, d, 1, 1, st));
+  if (dx_accum && dz) {
+    // dx = dz @ W_dn^T + dL @ Wr^T as one GEMM over K = l + E (overwrites dx)
+    MOE_REQUIRE(W_dn != nullptr && l > 0, MOE_ERR_ARG);
+    MOE_REQUIRE(l % 64 == 0 && al16(dz) && al16(W_dn), MOE_ERR_ALIGN);
+    GemmLaunch L;
+    L.name = "down_proj_router_dgrad";
+    L.BN = pick_bn(d);
+    L.sched = SCHED_DENSE;
+    L.M = T;
+    L.N = d;
+    L.K = l + E;
+    L.A = view(dz, T, l, l);
+    L.B = view(W_dn, d, l, l);      // B[n = d][k = l], K-major
+    L.kcat = l;
+    L.A2 = view(dL, T, E, E);
+    L.B2 = view(Wr, d, E, E);       // B2[n = d][k = E], K-major
+    L.epi = EPI_STORE;
+    L.C = dx_accum;
+    L.ldc = d;
+    L.c_bf16 = 1;
+    MOE_CHECK(gemm_launch(L, st));
+  } else if (dx_accum) {
+    MOE_CHECK(dense_gemm("router_dgrad", dL, E, 0, Wr, E, 0, T, d, E, dx_accum, d, 1, 1, st));
+  }
   if (dWr)
     MOE_CHECK(dense_gemm("router_wgrad", x, d, 1, dL, E, 1, d, E, T, dWr, E, wgrad_dtype == MOE_DTYPE_BF16, 0, st));
   return MOE_OK;

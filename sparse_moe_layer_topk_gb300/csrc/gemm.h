@@ -87,6 +87,11 @@ struct GemmLaunch {
   // operand of a grouped-K GEMM.
   const int* gather_idx = nullptr;
   int gather_a = 0, gather_b = 0;
+  // K concatenation (dense, K-major operands): for k >= kcat the A and B tiles
+  // come from A2 ([M][K-kcat]) and B2 ([N][K-kcat]): C = A B^T + A2 B2^T in one
+  // accumulator. kcat must be a multiple of 64.
+  int kcat = 0;
+  MatView A2, B2;
 };
 
 // Bytes of split workspace gemm_launch needs for M x N with `splitk` slices.

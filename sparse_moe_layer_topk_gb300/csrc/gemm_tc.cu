@@ -63,6 +63,7 @@ struct Params {
   int swiglu_b, f;
   int mt, nt;         // m tiles (dense / grouped-K), n tiles
   int splitk, kslice; // dense: K split into `splitk` slices of `kslice` (multiple of 64)
+  int kcat;           // dense: K index where A/B switch to the second operand pair (0: none)
   int total_static;   // tile count when it does not depend on device data
   int epi;
   void* C;
@@ -175,6 +176,7 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* err_f
 
 template <int BN, int EW, bool CW16, bool WARP>
 __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                              const CUtensorMap* mapA2, const CUtensorMap* mapB2,
                               uint8_t* smem, uint64_t* full, uint64_t* empty, int* sidx,
                               volatile int* abort_flag) {
   // WARP: run by the whole warp (the lanes fetch gather indices and issue the
@@ -237,6 +239,11 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
       }
       if (lane == 0) {
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+        if (p.kcat > 0 && k >= p.kcat) {
+          // second K segment: [A | A2] @ [B ; B2] (both K-major, dense)
+          tma_load_2d(sA, mapA2, &full[stage], k - p.kcat, ti.m0);
+          tma_load_2d(sB, mapB2, &full[stage], k - p.kcat, ti.nb0);
+        } else {
         // A
         if (!p.a_mn) {
           if (!gather_m) tma_load_2d(sA, mapA, &full[stage], k, ti.m0);
@@ -271,6 +278,7 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
             }
           }
         }
+        }  // first K segment
       }
       if (WARP) __syncwarp();
       ++issued;
@@ -877,7 +885,9 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC0,
-                   const __grid_constant__ CUtensorMap mapC1, const Params p) {
+                   const __grid_constant__ CUtensorMap mapC1,
+                   const __grid_constant__ CUtensorMap mapA2,
+                   const __grid_constant__ CUtensorMap mapB2, const Params p) {
   using C = Cfg<BN, EW, CW16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -921,9 +931,11 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     // Gathering launches run the producer on the whole warp (the lanes fetch
     // indices and issue gather4 copies); the others on lane 0 alone.
     if (p.gather_a || p.gather_b)
-      producer_loop<BN, EW, CW16, true>(p, &mapA, &mapB, smem, full, empty, sidx, abort_flag);
+      producer_loop<BN, EW, CW16, true>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty, sidx,
+                                        abort_flag);
     else if (lane_id() == 0)
-      producer_loop<BN, EW, CW16, false>(p, &mapA, &mapB, smem, full, empty, sidx, abort_flag);
+      producer_loop<BN, EW, CW16, false>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty, sidx,
+                                         abort_flag);
   } else if (warp == 1) {
     mma_loop<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
   } else {
@@ -1064,9 +1076,21 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   if (upper <= 0) return MOE_OK;
 
   if (!get_encoder()) return MOE_ERR_CUDA;
-  CUtensorMap mapA, mapB, mapC0, mapC1;
+  CUtensorMap mapA, mapB, mapC0, mapC1, mapA2, mapB2;
   memset(&mapC0, 0, sizeof(mapC0));
   memset(&mapC1, 0, sizeof(mapC1));
+  memset(&mapA2, 0, sizeof(mapA2));
+  memset(&mapB2, 0, sizeof(mapB2));
+  p.kcat = 0;
+  if (L.kcat > 0) {
+    // K-concatenated second operand pair: dense, both K-major, segment boundary on a K block
+    if (L.sched != SCHED_DENSE || L.a_mn || L.b_mn || L.b_batch_mode != BATCH_NONE ||
+        L.kcat % BK != 0 || L.splitk > 1 || L.gather_a || L.gather_b)
+      return MOE_ERR_UNSUPPORTED;
+    if (!make_map(&mapA2, L.A2, BM, false) || !make_map(&mapB2, L.B2, BN, false))
+      return MOE_ERR_ARG;
+    p.kcat = L.kcat;
+  }
   // gathered operands are read one row per box (tile::gather4)
   if (!make_map(&mapA, L.A, L.gather_a ? 1 : (L.a_mn ? 64 : BM), false)) return MOE_ERR_ARG;
   if (!make_map(&mapB, L.B, L.gather_b ? 1 : (L.b_mn ? 64 : BN), b3)) return MOE_ERR_ARG;
@@ -1124,8 +1148,8 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
   {
     LaunchTimer lt(L.name, stream);
-    gemm_tc_kernel<BN, EW, CW16><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mapA, mapB, mapC0,
-                                                                                mapC1, p);
+    gemm_tc_kernel<BN, EW, CW16><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
+        mapA, mapB, mapC0, mapC1, mapA2, mapB2, p);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -148,13 +148,14 @@ class LatentMoELayer:
                                 self.h_sh, T, l, f, S, self.dz_sh, g["W13_sh"], g["W2_sh"], wd,
                                 self.ws["sbwd"], self.ws_sizes["sbwd"], stream)
         M.moe_permute_bwd(self.dz_perm, self.slot_of, self.dz_sh, T, k, l, self.dz, stream)
-        M.moe_latent_proj_bwd(self.dz, self.x, w["W_dn"], T, d, l, self.dx, g["W_dn"], wd, stream)
+        # dW_dn here; dx = dz W_dn^T + dL Wr^T in the router backward's fused GEMM
+        M.moe_latent_proj_bwd(self.dz, self.x, w["W_dn"], T, d, l, None, g["W_dn"], wd, stream)
         aux = self.aux_scale > 0
         M.moe_route_topk_bwd(self.d_row_w, self.slot_of, self.topk_idx, self.topk_w, self.topk_s,
                              self.x, w["Wr"], T, d, E, k, self.d_topk_w, self.dx, g["Wr"], wd,
                              self.ws["route"] if aux else None, w.get("bias") if aux else None,
-                             self.p_mean if aux else None, self.aux_scale, self.ws["rbwd"],
-                             self.ws_sizes["rbwd"], self.err, stream)
+                             self.p_mean if aux else None, self.aux_scale, self.dz, w["W_dn"], l,
+                             self.ws["rbwd"], self.ws_sizes["rbwd"], self.err, stream)
         return self.dx
 
     def step(self, x, dout, stream=None):

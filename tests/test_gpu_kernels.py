@@ -315,7 +315,7 @@ def test_route_topk_bwd():
     M.moe_route_topk_bwd(dev(d_row_w), dev(torch.from_numpy(slot_of).int()),
                          dev(torch.from_numpy(idx).int()), dev(torch.from_numpy(w).float()),
                          dev(torch.from_numpy(s).float()), dev(x), dev(Wr), T, d, E, k, d_topk_w,
-                         dx_d, dWr, M.MOE_DTYPE_F32, None, None, None, 0.0, ws, wsb)
+                         dx_d, dWr, M.MOE_DTYPE_F32, None, None, None, 0.0, None, None, 0, ws, wsb)
     torch.cuda.synchronize()
     dw = f64(d_row_w)[slot_of]
     np.testing.assert_array_equal(d_topk_w.cpu().numpy(), d_row_w.numpy()[slot_of])
@@ -408,7 +408,8 @@ def test_router_aux_loss_and_gradient(T, E, bias):
     ones = torch.full((T, k), 0.25, dtype=torch.float32)
     M.moe_route_topk_bwd(dev(torch.zeros(T * k)), dev(torch.from_numpy(slot_of).int()),
                          dev(torch.from_numpy(idx).int()), dev(ones), dev(ones), dev(x), dev(Wr), T,
-                         d, E, k, None, None, dWr, M.MOE_DTYPE_F32, Ld, bd, p_mean, 3.0, ws2, wsb2)
+                         d, E, k, None, None, dWr, M.MOE_DTYPE_F32, Ld, bd, p_mean, 3.0, None, None,
+                         0, ws2, wsb2)
     torch.cuda.synchronize()
     dL = O.aux_balance_loss_backward(L.numpy(), b.numpy() if bias else None, scale=3.0)
     check_close("dWr_aux", f64(dWr), f64(x).T @ dL, scale_by_max=True)
@@ -466,3 +467,27 @@ def test_bucket_order_and_ordered_grouped_gemm(skew):
         torch.cuda.synchronize()
         outs.append((h.cpu().view(torch.int16), y.cpu().view(torch.int16)))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_route_topk_bwd_fused_down_projection_dgrad():
+    """dx = dz W_dn^T + dL Wr^T as one K-concatenated GEMM (K = l + E)."""
+    T, d, E, k, l = 500, 512, 128, 4, 256
+    x = _bf16(90, T, d)
+    Wr = _bf16(91, d, E, std=0.02)
+    W_dn = _bf16(92, d, l, std=0.02)
+    dz = _bf16(93, T, l)
+    L = O.router_logits(x, Wr)
+    idx = O.topk_select(L, k)
+    w, s = O.routing_weights(L, idx)
+    slot_of, _, _ = O.permutation_maps(idx, E)
+    d_row_w = torch.randn(T * k, generator=torch.Generator().manual_seed(9)).float()
+    dx = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    wsb = M.moe_workspace_size(M.MOE_OP_ROUTE_TOPK_BWD, T=T, E=E)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    M.moe_route_topk_bwd(dev(d_row_w), dev(torch.from_numpy(slot_of).int()),
+                         dev(torch.from_numpy(idx).int()), dev(torch.from_numpy(w).float()),
+                         dev(torch.from_numpy(s).float()), dev(x), dev(Wr), T, d, E, k, None, dx,
+                         None, M.MOE_DTYPE_F32, None, None, None, 0.0, dev(dz), dev(W_dn), l, ws, wsb)
+    torch.cuda.synchronize()
+    dL = O.router_backward(f64(d_row_w)[slot_of], w.astype(np.float32), s.astype(np.float32), idx, E)
+    check_close("dx", f64(dx), f64(dz) @ f64(W_dn).T + dL @ f64(Wr).T)
