@@ -47,10 +47,17 @@ struct Cfg {
                                             : ((EW == 8 && !CW16) ? 5 : 6);
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int THREADS = 64 + 32 * EW;
-  // per-warp output staging: 32-column blocks (one 4 KB fp32 block or three 2 KB
-  // bf16 blocks), or three 1 KB 16-column bf16 blocks (CW16: one stage more)
-  static constexpr int STG = CW16 ? 3072 : 6144;
+  // Per-warp output staging: what is left of the 227 KB after the operand
+  // stages (+ 1 KB alignment slack + 1 KB barriers), in whole KB, split into a
+  // ring of slots of one chunk's output each (4 KB fp32 or 2 KB bf16 for a
+  // 32-column block; SwiGLU chunks hold two or three blocks), so that a chunk's
+  // bulk store may still be reading its slot while the next chunks are staged.
+  static constexpr int SMEM_LIMIT = 232448;
+  static constexpr int STG_FIT = (SMEM_LIMIT - 2048 - STAGES * STAGE_BYTES) / EW / 1024 * 1024;
+  static constexpr int STG = STG_FIT > 16384 ? 16384 : STG_FIT;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * STG + 1024 + 1024;
+  static_assert(STG >= (CW16 ? 3072 : 6144), "staging must hold one chunk");
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
 };
 
 struct Params {
@@ -496,13 +503,27 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   const int grp = (warp - 2) / 4;
   const uint32_t lane = lane_id();
   const int r_loc = q * 32 + static_cast<int>(lane);
-  uint8_t* stg = staging + (warp - 2) * Cfg<BN, EW, CW16>::STG;
-  const uint32_t stg_s = smem_u32(stg);
+  uint8_t* const stg0 = staging + (warp - 2) * Cfg<BN, EW, CW16>::STG;
+  // slot of one chunk (1 KB multiples keep every swizzle span aligned)
+  int slot_bytes;
+  if (p.epi == EPI_STORE) slot_bytes = p.c_bf16 ? 2048 : 4096;
+  else if (p.epi == EPI_ROWSCALE) slot_bytes = 2048;
+  else if (p.epi == EPI_SWIGLU) slot_bytes = (CW16 ? 1024 : 2048) * (p.gu ? 3 : 1);
+  else slot_bytes = (CW16 ? 1024 : 2048) * (p.aux ? 3 : 2);
+  int nslots = Cfg<BN, EW, CW16>::STG / slot_bytes;
+  if (nslots > 4) nslots = 4;
+  int slot = 0;
+  uint8_t* stg = stg0;  // the current chunk's slot (set by stage_begin)
+  uint32_t stg_s = smem_u32(stg0);
   const int total = total_tiles(p);
-  bool pending = false;  // a bulk store of this warp may still read the staging area
+  bool pending = false;  // a bulk store of this warp may still read a slot
   auto stage_begin = [&]() {
+    stg = stg0 + slot * slot_bytes;
+    stg_s = smem_u32(stg);
+    if (++slot == nslots) slot = 0;
     if (pending) {
-      if (lane == 0) bulk_wait_read_all();
+      // the store that last used this slot was committed nslots groups ago
+      if (lane == 0) bulk_wait_read_max(nslots - 1);
       __syncwarp();
     }
   };
