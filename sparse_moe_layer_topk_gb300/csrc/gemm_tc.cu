@@ -353,20 +353,27 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
       }
       tc_fence_after();
       uint8_t* sA = smem + stage * C::STAGE_BYTES;
+      int nkk = BK / 16;  // K=16 MMAs of this block
       if (p.sched == SCHED_GROUPED_K) {
         const int valid = ti.krows - kb * BK;
         if (valid < BK) {
-          // Rows past this expert's segment belong to the next expert: zero them
-          // in every 64-wide chunk of A and B (rows are whole 128-byte lines).
-          const int n16 = (BK - valid) * 8;  // 16-byte pieces per chunk
-          const uint4 zero = make_uint4(0, 0, 0, 0);
+          // Rows past this expert's segment belong to the next expert. The MMAs
+          // wholly past the segment are skipped; the rows of the last one that
+          // lie past it are zeroed in every 64-wide chunk of A and B (rows are
+          // whole 128-byte lines).
+          nkk = (valid + 15) >> 4;
+          const int nz = nkk * 16 - valid;
+          if (nz > 0) {
+            const int n16 = nz * 8;  // 16-byte pieces per chunk
+            const uint4 zero = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int c = 0; c < 2 + BN / 64; ++c) {
-            uint8_t* base = sA + c * CHUNK_BYTES + valid * 128;
-            for (int i = lane; i < n16; i += 32)
-              *reinterpret_cast<uint4*>(base + (i >> 3) * 128 + (i & 7) * 16) = zero;
+            for (int c = 0; c < 2 + BN / 64; ++c) {
+              uint8_t* base = sA + c * CHUNK_BYTES + valid * 128;
+              for (int i = lane; i < n16; i += 32)
+                *reinterpret_cast<uint4*>(base + (i >> 3) * 128 + (i & 7) * 16) = zero;
+            }
+            fence_proxy_async_smem();
           }
-          fence_proxy_async_smem();
         }
       }
       __syncwarp();
@@ -374,9 +381,11 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
         const uint32_t a0 = smem_u32(sA), b0 = a0 + A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = make_sdesc(a0 + kk * a_kstep, a_lbo, 1024);
-          const uint64_t bd = make_sdesc(b0 + kk * b_kstep, b_lbo, 1024);
-          mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          if (kk < nkk) {
+            const uint64_t ad = make_sdesc(a0 + kk * a_kstep, a_lbo, 1024);
+            const uint64_t bd = make_sdesc(b0 + kk * b_kstep, b_lbo, 1024);
+            mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
         }
         mma_commit(&empty[stage]);
       }
