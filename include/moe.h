@@ -270,7 +270,10 @@ int moe_unpermute_combine_bwd(const uint16_t* dy_lat, const int32_t* token_of, i
  *   dW2[e]    = sum_r (row_w[r] h[r])^T dy_perm[r]                  ([E][f][l])
  *   dW13[e]   = sum_r z_perm[r]^T [dg|du][r]                         ([E][l][2f])
  * dW13/dW2 are fp32 or bf16 per wgrad_dtype; an expert with no rows gets exact
- * zeros. gu_save and h from the forward are required. Workspace:
+ * zeros. The weight gradients of expert e read no more than a few of the rows
+ * that follow its segment, multiplied by zero: they are exact as long as every
+ * row of dy_perm / [dg|du] is finite (a non-finite row of expert e+1 may also
+ * turn dW of expert e into NaN). gu_save and h from the forward are required. Workspace:
  * moe_workspace_size(MOE_OP_GROUPED_SWIGLU_BWD, 0, 0, l, E, 0, f, 0) with T*k = R
  * passed as T (k = 1). */
 int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, const uint16_t* W13,

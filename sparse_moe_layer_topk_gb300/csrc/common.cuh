@@ -113,6 +113,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint6
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint64_t* bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // Four rows of a 2-D tensor (box of one row) gathered by row index into four
 // consecutive 128-byte rows of shared memory (sm_100 tile::gather4 mode).
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, uint64_t* bar, int col,

@@ -66,6 +66,9 @@ struct Params {
   const int* tile_sched;
   const int* expert_order;  // grouped-M: position -> group (nullptr: identity)
   int a_mn, b_mn, b_rank3;
+  // MN-major operand read through a chunked map ([batch][cols/64][rows][64]):
+  // all of a tile's 64-column chunks in one copy instead of one copy per chunk
+  int a_chunked, b_chunked;
   int b_batch_mode, n_tiles_per_batch, k_per_batch;
   int swiglu_b, f;
   int mt, nt;         // m tiles (dense / grouped-K), n tiles
@@ -255,8 +258,12 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
         if (!p.a_mn) {
           if (!gather_m) tma_load_2d(sA, mapA, &full[stage], k, ti.m0);
         } else if (!(gather_k && p.gather_a)) {
-          tma_load_2d(sA, mapA, &full[stage], ti.m0, k);
-          tma_load_2d(sA + CHUNK_BYTES, mapA, &full[stage], ti.m0 + 64, k);
+          if (p.a_chunked) {
+            tma_load_3d(sA, mapA, &full[stage], 0, k, ti.m0 >> 6);
+          } else {
+            tma_load_2d(sA, mapA, &full[stage], ti.m0, k);
+            tma_load_2d(sA + CHUNK_BYTES, mapA, &full[stage], ti.m0 + 64, k);
+          }
         }
         // B
         int kb_coord = k, batch = ti.batch;
@@ -267,6 +274,16 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
         if (!p.b_mn) {
           if (p.b_rank3) tma_load_3d(sB, mapB, &full[stage], kb_coord, ti.nb0, batch);
           else tma_load_2d(sB, mapB, &full[stage], kb_coord, ti.nb0);
+        } else if (p.b_chunked) {
+          // one copy per run of consecutive chunks: the whole tile, or its gate
+          // and up halves (columns nb0 and f + nb0) for the SwiGLU pair
+          const int nruns = p.swiglu_b ? 2 : 1;
+          for (int r = 0; r < nruns; ++r) {
+            const int c0 = (r == 0 ? ti.nb0 : p.f + ti.nb0) >> 6;
+            const uint32_t dst = sB + r * (BN / 2) * 128;
+            if (p.b_rank3) tma_load_4d(dst, mapB, &full[stage], 0, kb_coord, c0, batch);
+            else tma_load_3d(dst, mapB, &full[stage], 0, kb_coord, c0);
+          }
         } else {
 #pragma unroll
           for (int c = 0; c < BN / 64; ++c) {
@@ -357,17 +374,18 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
       if (p.sched == SCHED_GROUPED_K) {
         const int valid = ti.krows - kb * BK;
         if (valid < BK) {
-          // Rows past this expert's segment belong to the next expert. The MMAs
-          // wholly past the segment are skipped; the rows of the last one that
-          // lie past it are zeroed in every 64-wide chunk of A and B (rows are
-          // whole 128-byte lines).
+          // Rows past this expert's segment belong to the next expert (or are
+          // repeats of its last row, or zero fill past the tensor). The MMAs
+          // wholly past the segment are skipped; in the last one the rows past
+          // it are zeroed in A's two 64-wide chunks (rows are whole 128-byte
+          // lines), so that they add 0 * (finite B row) = 0.
           nkk = (valid + 15) >> 4;
           const int nz = nkk * 16 - valid;
           if (nz > 0) {
             const int n16 = nz * 8;  // 16-byte pieces per chunk
             const uint4 zero = make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int c = 0; c < 2 + BN / 64; ++c) {
+            for (int c = 0; c < BM / 64; ++c) {
               uint8_t* base = sA + c * CHUNK_BYTES + valid * 128;
               for (int i = lane; i < n16; i += 32)
                 *reinterpret_cast<uint4*>(base + (i >> 3) * 128 + (i & 7) * 16) = zero;
@@ -1013,6 +1031,26 @@ bool make_map(CUtensorMap* map, const MatView& v, int box_rows, bool force3d) {
   return r == CUDA_SUCCESS;
 }
 
+// Chunked map of an MN-major bf16 operand [batch][rows][cols] (cols a multiple
+// of 64): dimensions {64, rows, cols/64 (, batch)}, box {64, 64, nchunks (, 1)}.
+// One copy lands `nchunks` 64-column blocks at 8 KB strides in shared memory,
+// the layout that `nchunks` separate {64, 64} boxes of the plain map give.
+bool make_map_chunked(CUtensorMap* map, const MatView& v, int nchunks, bool force4d) {
+  if (v.cols % 64 != 0) return false;
+  const bool rank4 = force4d || v.batch > 1;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(v.rows), static_cast<cuuint64_t>(v.cols / 64),
+                        static_cast<cuuint64_t>(v.batch)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(v.ld) * 2, 128,
+                           static_cast<cuuint64_t>(v.batch_stride) * 2};
+  cuuint32_t box[4] = {64, 64, static_cast<cuuint32_t>(nchunks), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank4 ? 4 : 3,
+                        const_cast<void*>(v.ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Tensor map of an output tensor [d2][d1][d0] (d0 contiguous) for 32x32-element
 // TMA stores: bf16 rows of 64 bytes with 64-byte swizzle, fp32 rows of 128 bytes
 // with 128-byte swizzle (the layouts stage_bf16 / stage_f32 write).
@@ -1121,9 +1159,18 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
       return MOE_ERR_ARG;
     p.kcat = L.kcat;
   }
-  // gathered operands are read one row per box (tile::gather4)
-  if (!make_map(&mapA, L.A, L.gather_a ? 1 : (L.a_mn ? 64 : BM), false)) return MOE_ERR_ARG;
-  if (!make_map(&mapB, L.B, L.gather_b ? 1 : (L.b_mn ? 64 : BN), b3)) return MOE_ERR_ARG;
+  // gathered operands are read one row per box (tile::gather4); other MN-major
+  // operands through a chunked map when their columns allow (else one copy per
+  // 64-column chunk)
+  // (the chunk coordinate is m0 / 64: grouped-M row starts are not 64-aligned)
+  p.a_chunked = L.a_mn && !L.gather_a && L.sched != SCHED_GROUPED_M &&
+                make_map_chunked(&mapA, L.A, BM / 64, false);
+  p.b_chunked = L.b_mn && !L.gather_b &&
+                make_map_chunked(&mapB, L.B, L.swiglu_b ? BN / 128 : BN / 64, b3);
+  if (!p.a_chunked && !make_map(&mapA, L.A, L.gather_a ? 1 : (L.a_mn ? 64 : BM), false))
+    return MOE_ERR_ARG;
+  if (!p.b_chunked && !make_map(&mapB, L.B, L.gather_b ? 1 : (L.b_mn ? 64 : BN), b3))
+    return MOE_ERR_ARG;
   // output (store) maps
   const long long rows_out = (L.sched == SCHED_GROUPED_M) ? L.R_cap : L.M;
   bool ok = true;
