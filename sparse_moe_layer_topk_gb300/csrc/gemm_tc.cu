@@ -36,6 +36,10 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int CHUNK_BYTES = 64 * 128;  // one 64-row x 128-byte swizzled block
+// Per-CTA table of decoded grouped tiles (16 bytes each), filled at kernel start
+// so that no role walks the tile schedule in global memory between tiles.
+constexpr int TILE_TABLE_BYTES = 4096;
+constexpr int TILE_TABLE_CAP = TILE_TABLE_BYTES / 16;
 
 // BN: tile width (UMMA N); EW: epilogue warps (4, or 8 for heavy epilogues:
 // two warps per TMEM lane quadrant, splitting the tile's column chunks).
@@ -53,9 +57,10 @@ struct Cfg {
   // 32-column block; SwiGLU chunks hold two or three blocks), so that a chunk's
   // bulk store may still be reading its slot while the next chunks are staged.
   static constexpr int SMEM_LIMIT = 232448;
-  static constexpr int STG_FIT = (SMEM_LIMIT - 2048 - STAGES * STAGE_BYTES) / EW / 1024 * 1024;
+  static constexpr int STG_FIT =
+      (SMEM_LIMIT - 2048 - TILE_TABLE_BYTES - STAGES * STAGE_BYTES) / EW / 1024 * 1024;
   static constexpr int STG = STG_FIT > 16384 ? 16384 : STG_FIT;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * STG + 1024 + 1024;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * STG + 1024 + 1024 + TILE_TABLE_BYTES;
   static_assert(STG >= (CW16 ? 3072 : 6144), "staging must hold one chunk");
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
 };
@@ -182,13 +187,51 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* err_f
   set_flag(err_flag, MOE_FLAG_TIMEOUT);
 }
 
+// Table entry of a grouped tile: grouped-M {g, m0, rows, n_blk}; grouped-K
+// {g, n_blk << 16 | m_blk, k0, krows}.
+template <int BN>
+__device__ __forceinline__ int4 pack_tile(const Params& p, const Tile& ti) {
+  if (p.sched == SCHED_GROUPED_M) return make_int4(ti.g, ti.m0, ti.rows, ti.n_blk);
+  return make_int4(ti.g, (ti.n_blk << 16) | (ti.m0 / BM), ti.k0, ti.krows);
+}
+
+// The i-th tile (t = blockIdx.x + i * gridDim.x) of this CTA: from the table when
+// it holds it, else decoded from the schedule.
+template <int BN>
+__device__ __forceinline__ Tile tile_of(const Params& p, const int4* ttab, int i, int t) {
+  if (p.sched == SCHED_DENSE || i >= TILE_TABLE_CAP) return decode<BN>(p, t);
+  const int4 e = ttab[i];
+  const int bn_eff = p.swiglu_b ? BN / 2 : BN;
+  Tile ti;
+  ti.g = e.x;
+  if (p.sched == SCHED_GROUPED_M) {
+    ti.m0 = e.y;
+    ti.rows = e.z;
+    ti.n_blk = e.w;
+    ti.batch = e.x;
+    ti.k0 = 0;
+    ti.krows = p.K;
+    ti.nk = (p.K + BK - 1) / BK;
+  } else {
+    ti.n_blk = e.y >> 16;
+    ti.m0 = (e.y & 0xFFFF) * BM;
+    ti.rows = min(BM, p.M - ti.m0);
+    ti.batch = 0;
+    ti.k0 = e.z;
+    ti.krows = e.w;
+    ti.nk = (e.w + BK - 1) / BK;
+  }
+  ti.nb0 = ti.n_blk * bn_eff;
+  return ti;
+}
+
 // ------------------------------------------------------------------ producer
 
 template <int BN, int EW, bool CW16, bool WARP>
 __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CUtensorMap* mapB,
                               const CUtensorMap* mapA2, const CUtensorMap* mapB2,
                               uint8_t* smem, uint64_t* full, uint64_t* empty, int* sidx,
-                              volatile int* abort_flag) {
+                              const int4* ttab, volatile int* abort_flag) {
   // WARP: run by the whole warp (the lanes fetch gather indices and issue the
   // gather4 copies, lane 0 the others); otherwise by lane 0 alone.
   using C = Cfg<BN, EW, CW16>;
@@ -200,8 +243,9 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
   const bool gather_m = WARP && p.gather_a && p.sched == SCHED_GROUPED_M;
   const bool gather_k = WARP && (p.gather_a || p.gather_b) && p.sched == SCHED_GROUPED_K;
   bool ok = true;
-  for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-    const Tile ti = decode<BN>(p, t);
+  int it = 0;
+  for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+    const Tile ti = tile_of<BN>(p, ttab, it, t);
     if (gather_m) {
       // source rows of the tile's 128 A rows; rows past the expert's segment
       // repeat its last row (their results are never stored)
@@ -340,7 +384,7 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
 template <int BN, int EW, bool CW16>
 __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                          uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
-                         volatile int* abort_flag) {
+                         const int4* ttab, volatile int* abort_flag) {
   using C = Cfg<BN, EW, CW16>;
   const uint32_t lane = lane_id();
   const uint32_t idesc = make_idesc_bf16(BM, BN, p.a_mn, p.b_mn);
@@ -353,7 +397,7 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   int it = 0;
   bool ok = true;
   for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-    const Tile ti = decode<BN>(p, t);
+    const Tile ti = tile_of<BN>(p, ttab, it, t);
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
     if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
@@ -523,7 +567,7 @@ struct StoreMaps {
 template <int BN, int EW, bool CW16>
 __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* staging,
                               uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base,
-                              volatile int* abort_flag) {
+                              const int4* ttab, volatile int* abort_flag) {
   constexpr int NG = EW / 4;  // warps per TMEM lane quadrant; they split the column chunks
   const int warp = threadIdx.x >> 5;
   const int q = warp & 3;  // tensor-memory lane quadrant this warp may read
@@ -560,7 +604,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   };
   int it = 0;
   for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-    const Tile ti = decode<BN>(p, t);
+    const Tile ti = tile_of<BN>(p, ttab, it, t);
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
     if (!mbar_wait(&tfull[buf], use & 1u, abort_flag)) {
@@ -949,7 +993,18 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* sidx = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 256);  // 128 gather indices
+  int4* ttab = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(full) + 1024);
   const int warp = threadIdx.x >> 5;
+  if (p.sched != SCHED_DENSE && warp >= 2) {
+    // the epilogue warps decode this CTA's first TILE_TABLE_CAP tiles in parallel
+    const int total = total_tiles(p);
+    const int mine = total > static_cast<int>(blockIdx.x)
+                         ? (total - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
+                         : 0;
+    const int n = mine < TILE_TABLE_CAP ? mine : TILE_TABLE_CAP;
+    for (int i = threadIdx.x - 64; i < n; i += 32 * EW)
+      ttab[i] = pack_tile<BN>(p, decode<BN>(p, blockIdx.x + i * gridDim.x));
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -980,15 +1035,15 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     // indices and issue gather4 copies); the others on lane 0 alone.
     if (p.gather_a || p.gather_b)
       producer_loop<BN, EW, CW16, true>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty, sidx,
-                                        abort_flag);
+                                        ttab, abort_flag);
     else if (lane_id() == 0)
       producer_loop<BN, EW, CW16, false>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty, sidx,
-                                         abort_flag);
+                                         ttab, abort_flag);
   } else if (warp == 1) {
-    mma_loop<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
+    mma_loop<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base, ttab, abort_flag);
   } else {
     const StoreMaps sm{&mapC0, &mapC1, p.c0_rank3};
-    epilogue_loop<BN, EW, CW16>(p, sm, staging, tfull, tempty, tmem_base, abort_flag);
+    epilogue_loop<BN, EW, CW16>(p, sm, staging, tfull, tempty, tmem_base, ttab, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
