@@ -36,10 +36,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int CHUNK_BYTES = 64 * 128;  // one 64-row x 128-byte swizzled block
-// Per-CTA table of decoded grouped tiles (16 bytes each), filled at kernel start
-// so that no role walks the tile schedule in global memory between tiles.
-constexpr int TILE_TABLE_BYTES = 4096;
-constexpr int TILE_TABLE_CAP = TILE_TABLE_BYTES / 16;
+constexpr int MISC_BYTES = 768;  // barriers (256 B) + 128 gather row indices (512 B)
 
 // BN: tile width (UMMA N); EW: epilogue warps (4, or 8 for heavy epilogues:
 // two warps per TMEM lane quadrant, splitting the tile's column chunks).
@@ -51,17 +48,23 @@ struct Cfg {
                                             : ((EW == 8 && !CW16) ? 5 : 6);
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int THREADS = 64 + 32 * EW;
-  // Per-warp output staging: what is left of the 227 KB after the operand
-  // stages (+ 1 KB alignment slack + 1 KB barriers), in whole KB, split into a
-  // ring of slots of one chunk's output each (4 KB fp32 or 2 KB bf16 for a
-  // 32-column block; SwiGLU chunks hold two or three blocks), so that a chunk's
-  // bulk store may still be reading its slot while the next chunks are staged.
+  // Per-warp output staging, a ring of slots of one chunk's output each (4 KB
+  // fp32 or 2 KB bf16 for a 32-column block; SwiGLU chunks hold two or three
+  // blocks), so that a chunk's bulk store may still be reading its slot while
+  // the next chunks are staged: one fp32 / three bf16 slots with 4 epilogue
+  // warps (a whole tile table of a ragged-K weight gradient measured faster
+  // than a second fp32 slot), one SwiGLU chunk with 8.
+  static constexpr int STG = CW16 ? 3072 : (EW == 8 ? 6144 : 7168);
+  // The rest of the 227 KB (after 1 KB alignment slack and the barriers) holds
+  // the CTA's table of decoded grouped tiles, 16 bytes per tile.
   static constexpr int SMEM_LIMIT = 232448;
-  static constexpr int STG_FIT =
-      (SMEM_LIMIT - 2048 - TILE_TABLE_BYTES - STAGES * STAGE_BYTES) / EW / 1024 * 1024;
-  static constexpr int STG = STG_FIT > 16384 ? 16384 : STG_FIT;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * STG + 1024 + 1024 + TILE_TABLE_BYTES;
-  static_assert(STG >= (CW16 ? 3072 : 6144), "staging must hold one chunk");
+  static constexpr int TT_FIT =
+      (SMEM_LIMIT - 1024 - MISC_BYTES - STAGES * STAGE_BYTES - EW * STG) / 16 * 16;
+  static constexpr int TT_BYTES = TT_FIT > 16384 ? 16384 : TT_FIT;
+  static constexpr int TT_CAP = TT_BYTES / 16;
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + EW * STG + 1024 + MISC_BYTES + TT_BYTES;
+  static_assert(TT_CAP >= 64, "tile table");
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
 };
 
@@ -196,10 +199,10 @@ __device__ __forceinline__ int4 pack_tile(const Params& p, const Tile& ti) {
 }
 
 // The i-th tile (t = blockIdx.x + i * gridDim.x) of this CTA: from the table when
-// it holds it, else decoded from the schedule.
+// it holds it (the first `cap` tiles), else decoded from the schedule.
 template <int BN>
-__device__ __forceinline__ Tile tile_of(const Params& p, const int4* ttab, int i, int t) {
-  if (p.sched == SCHED_DENSE || i >= TILE_TABLE_CAP) return decode<BN>(p, t);
+__device__ __forceinline__ Tile tile_of(const Params& p, const int4* ttab, int cap, int i, int t) {
+  if (p.sched == SCHED_DENSE || i >= cap) return decode<BN>(p, t);
   const int4 e = ttab[i];
   const int bn_eff = p.swiglu_b ? BN / 2 : BN;
   Tile ti;
@@ -245,7 +248,7 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
   bool ok = true;
   int it = 0;
   for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-    const Tile ti = tile_of<BN>(p, ttab, it, t);
+    const Tile ti = tile_of<BN>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
     if (gather_m) {
       // source rows of the tile's 128 A rows; rows past the expert's segment
       // repeat its last row (their results are never stored)
@@ -397,7 +400,7 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   int it = 0;
   bool ok = true;
   for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-    const Tile ti = tile_of<BN>(p, ttab, it, t);
+    const Tile ti = tile_of<BN>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
     if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
@@ -604,7 +607,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   };
   int it = 0;
   for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-    const Tile ti = tile_of<BN>(p, ttab, it, t);
+    const Tile ti = tile_of<BN>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
     if (!mbar_wait(&tfull[buf], use & 1u, abort_flag)) {
@@ -993,15 +996,15 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* sidx = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 256);  // 128 gather indices
-  int4* ttab = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(full) + 1024);
+  int4* ttab = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(full) + MISC_BYTES);
   const int warp = threadIdx.x >> 5;
   if (p.sched != SCHED_DENSE && warp >= 2) {
-    // the epilogue warps decode this CTA's first TILE_TABLE_CAP tiles in parallel
+    // the epilogue warps decode this CTA's first TT_CAP tiles in parallel
     const int total = total_tiles(p);
     const int mine = total > static_cast<int>(blockIdx.x)
                          ? (total - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
                          : 0;
-    const int n = mine < TILE_TABLE_CAP ? mine : TILE_TABLE_CAP;
+    const int n = mine < C::TT_CAP ? mine : C::TT_CAP;
     for (int i = threadIdx.x - 64; i < n; i += 32 * EW)
       ttab[i] = pack_tile<BN>(p, decode<BN>(p, blockIdx.x + i * gridDim.x));
   }

@@ -282,38 +282,51 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   }
 }
 
-// One warp per token; each lane owns up to 4 16-byte column vectors per pass.
-__global__ void __launch_bounds__(256) gather_sum_kernel(const uint4* __restrict__ src,
-                                                         const int* __restrict__ slot, int k,
-                                                         const uint4* __restrict__ add, int T,
-                                                         int nvec, uint4* __restrict__ out,
-                                                         long long ld_out_vec) {
+// One warp per token: lane j reads slot j of the token once; the rows are
+// summed four at a time (their loads issued together, the sums taken in slot
+// order), each lane owning up to 4 16-byte column vectors per pass.
+__global__ void __launch_bounds__(256, 2) gather_sum_kernel(const uint4* __restrict__ src,
+                                                            const int* __restrict__ slot, int k,
+                                                            const uint4* __restrict__ add, int T,
+                                                            int nvec, uint4* __restrict__ out,
+                                                            long long ld_out_vec) {
+  constexpr int U = 4;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
+  const int my_slot = lane < k ? __ldg(slot + static_cast<size_t>(t) * k + lane) : -1;
+  const uint4 z4 = make_uint4(0, 0, 0, 0);
   for (int v0 = 0; v0 < nvec; v0 += 128) {
     float acc[4][8];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const int r = __ldg(slot + static_cast<size_t>(t) * k + j);
-      if (r < 0) continue;
-      const uint4* s = src + static_cast<long long>(r) * nvec;
-      uint4 x[4];
+    for (int j0 = 0; j0 < k; j0 += U) {
+      int r[U];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int v = v0 + lane + 32 * i;
-        x[i] = (v < nvec) ? __ldg(s + v) : make_uint4(0, 0, 0, 0);
-      }
+      for (int u = 0; u < U; ++u) r[u] = __shfl_sync(0xFFFFFFFFu, my_slot, (j0 + u) & 31);
+      uint4 x[U][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t wv[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+      for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[i][2 * e] += bf16_lo(wv[e]);
-          acc[i][2 * e + 1] += bf16_hi(wv[e]);
+        for (int i = 0; i < 4; ++i) {
+          const int v = v0 + lane + 32 * i;
+          x[u][i] = (j0 + u < k && r[u] >= 0 && v < nvec)
+                        ? __ldg(src + static_cast<long long>(r[u]) * nvec + v)
+                        : z4;
+        }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (j0 + u >= k || r[u] < 0) continue;  // warp-uniform
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t wv[4] = {x[u][i].x, x[u][i].y, x[u][i].z, x[u][i].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[i][2 * e] += bf16_lo(wv[e]);
+            acc[i][2 * e + 1] += bf16_hi(wv[e]);
+          }
         }
       }
     }
