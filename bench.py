@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of CUDA-graph replays of the step")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the secondary workloads (T=4096 forward uniform / Zipf, EP rank)")
     ap.add_argument("--tokens", type=int, default=0,
@@ -398,29 +400,47 @@ def run_ours(args):
     except Exception:
         dev_uuid = str(local)
     clocks = ClockSampler(dev_uuid)
-    M.moe_timing_report()  # drop anything recorded so far
-    M.moe_timing_enable(True)
+    graph = None
+    if not args.no_graph:
+        # the step as one CUDA graph (no host launch gaps), replayed K times
+        graph = layer.capture_step(x, g)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    def timed(fn, per_kernel_events):
+        M.moe_timing_report()  # drop anything recorded so far
+        M.moe_timing_enable(per_kernel_events)
+        barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        M.moe_timing_enable(False)
+        rep = M.moe_timing_report()
+        t_ms = ev0.elapsed_time(ev1)
+        if world > 1:
+            t = torch.tensor([t_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_ms = float(t.item())
+        return t_ms, rep
+
     clocks.start()
-    barrier()
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        layer.step(x, g)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
+    # per-kernel CUDA events over K eager steps (launch durations for the roofline)
+    ms_eager, per_kernel = timed(lambda: layer.step(x, g), True)
+    if graph is not None:
+        ms, _ = timed(graph.replay, False)
+    else:
+        ms = ms_eager
     clk = clocks.stop()
-    M.moe_timing_enable(False)
-    per_kernel = M.moe_timing_report()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    timing_desc = "CUDA-graph replays of the step" if graph is not None else "eager launches"
     value = world * T * args.steps / (ms / 1000.0)
-    launches = sum(c for c, _ in per_kernel.values())
+    launches = sum(c for c, _ in per_kernel.values())  # the same kernels, once per step
 
     # ---- end to end: pinned host inputs in, input gradient out, every step
     e2e = None
@@ -428,7 +448,8 @@ def run_ours(args):
         xh = inp["x"].pin_memory()
         gh = inp["g"].pin_memory()
         dxh = torch.empty_like(xh).pin_memory()
-        layer.steps_from_host([xh] * 2, [gh] * 2, [dxh] * 2)  # warm the copy pipeline
+        use_graphs = not args.no_graph
+        layer.steps_from_host([xh] * 2, [gh] * 2, [dxh] * 2, graphs=use_graphs)  # warm up
         barrier()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -436,7 +457,8 @@ def run_ours(args):
         e0.record(stream)
         # every step copies its x and dout in from pinned host memory and its dx
         # out; the copies overlap the neighbouring steps' compute
-        layer.steps_from_host([xh] * args.steps, [gh] * args.steps, [dxh] * args.steps)
+        layer.steps_from_host([xh] * args.steps, [gh] * args.steps, [dxh] * args.steps,
+                              graphs=use_graphs)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -490,7 +512,7 @@ def run_ours(args):
 
     secondary = None
     if rank == 0 and not args.no_secondary and not (args.tokens or args.experts):
-        del layer
+        del layer, graph
         torch.cuda.empty_cache()
         secondary = secondary_workloads(20, 3, tc)
 
@@ -519,6 +541,9 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
+            "timing": {"value": timing_desc,
+                       "kernels": "CUDA events around every launch over K eager steps",
+                       "ms_per_step_eager": ms_eager / args.steps},
             "clocks": clk,
             "kernels": breakdown,
         }

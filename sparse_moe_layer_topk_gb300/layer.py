@@ -162,7 +162,17 @@ class LatentMoELayer:
         self.forward(x, stream)
         return self.backward(dout, stream)
 
-    def steps_from_host(self, x_host, g_host, dx_host):
+    def capture_step(self, x, dout):
+        """Records one forward + backward on the fixed buffers x and dout as a
+        CUDA graph; graph.replay() reruns it on the current stream. A step
+        allocates nothing and never waits on the host, so it captures whole (run
+        one eager step first: the library sets its kernels' attributes then)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(x, dout)
+        return g
+
+    def steps_from_host(self, x_host, g_host, dx_host, graphs: bool = True):
         """Forward + backward for each (x, dout) pair of pinned host tensors,
         writing each step's input gradient back to the pinned dx_host[i].
 
@@ -170,7 +180,8 @@ class LatentMoELayer:
         run on their own streams (separate copy engines) while step i computes;
         device inputs and input gradients are double-buffered and ordered with
         events, so every step still copies its own inputs in and its gradient
-        out. Returns after the last copy has been enqueued; synchronise the
+        out. With graphs, each slot's step is a CUDA graph captured on first
+        use. Returns after the last copy has been enqueued; synchronise the
         current stream's device to wait for the results."""
         n = len(x_host)
         assert len(g_host) == n and len(dx_host) == n
@@ -185,6 +196,13 @@ class LatentMoELayer:
                 "dx": [torch.empty_like(self.dx) for _ in range(2)],
             }
         P = self._pipe
+        if graphs and not hasattr(self, "_pipe_graphs"):
+            keep = self.dx
+            self._pipe_graphs = []
+            for s in range(2):
+                self.dx = P["dx"][s]
+                self._pipe_graphs.append(self.capture_step(P["x"][s], P["g"][s]))
+            self.dx = keep
         ev = lambda: torch.cuda.Event()  # noqa: E731
         loaded = [None] * n
         computed = [None] * n
@@ -208,9 +226,12 @@ class LatentMoELayer:
             comp.wait_event(loaded[i])
             if i >= 2:
                 comp.wait_event(drained[i - 2])  # dx slot s copied out by step i-2
-            self.forward(P["x"][s])
-            self.dx = P["dx"][s]  # the backward writes the input gradient into slot s
-            self.backward(P["g"][s])
+            if graphs:
+                self._pipe_graphs[s].replay()
+            else:
+                self.forward(P["x"][s])
+                self.dx = P["dx"][s]  # the backward writes the input gradient into slot s
+                self.backward(P["g"][s])
             computed[i] = ev()
             computed[i].record(comp)
             with torch.cuda.stream(d2h):

@@ -229,9 +229,11 @@ def test_layer_cfg0_with_aux_balance_loss():
     check_close("dWr", f64(layer.grads["Wr"]), bwd["dWr"] + x.T @ dL_aux, scale_by_max=True)
 
 
-def test_steps_from_host_pipeline_matches_step():
+@pytest.mark.parametrize("graphs", [True, False])
+def test_steps_from_host_pipeline_matches_step(graphs):
     """The pipelined host-driven steps (copies on their own streams, double-
-    buffered device inputs) give the same input gradients as plain steps."""
+    buffered device inputs, CUDA-graph replays or eager launches) give the same
+    input gradients as plain steps."""
     inp = I.make_layer_inputs(0)
     cfg = inp["cfg"]
     layer = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32)
@@ -239,10 +241,36 @@ def test_steps_from_host_pipeline_matches_step():
     xs = [torch.randn(cfg.T, cfg.d, generator=g0).to(torch.bfloat16).pin_memory() for _ in range(3)]
     gs = [torch.randn(cfg.T, cfg.d, generator=g0).to(torch.bfloat16).pin_memory() for _ in range(3)]
     outs = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
-    layer.steps_from_host(xs, gs, outs)
+    layer.steps_from_host(xs, gs, outs, graphs=graphs)
     torch.cuda.synchronize()
     ref = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32)
     for i in range(3):
         dx = ref.step(xs[i].cuda(), gs[i].cuda())
         torch.cuda.synchronize()
         assert torch.equal(dx.cpu(), outs[i]), i
+
+
+def test_captured_step_replays_bit_identical():
+    """A step captured as a CUDA graph and replayed on new contents of its input
+    buffers gives the eager step's outputs and gradients bit for bit."""
+    inp = I.make_layer_inputs(0)
+    cfg = inp["cfg"]
+    layer = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32)
+    x = inp["x"].cuda()
+    g = inp["g"].cuda()
+    layer.step(x, g)  # eager first: kernel attributes are set outside the capture
+    graph = layer.capture_step(x, g)
+    gen = torch.Generator().manual_seed(21)
+    x.copy_(torch.randn(cfg.T, cfg.d, generator=gen).to(torch.bfloat16))
+    g.copy_(torch.randn(cfg.T, cfg.d, generator=gen).to(torch.bfloat16))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(layer.err.item()) == 0
+    got = {"out": layer.out.clone(), "dx": layer.dx.clone(),
+           **{n: t.clone() for n, t in layer.grads.items()}}
+    ref = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32)
+    ref.step(x, g)
+    torch.cuda.synchronize()
+    want = {"out": ref.out, "dx": ref.dx, **ref.grads}
+    for n in got:
+        assert torch.equal(got[n], want[n]), n
