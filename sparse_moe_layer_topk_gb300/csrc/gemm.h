@@ -92,6 +92,9 @@ struct GemmLaunch {
   // accumulator. kcat must be a multiple of 64.
   int kcat = 0;
   MatView A2, B2;
+  // Dense schedule with 256-wide tiles: run CTA pairs on 256-row tiles
+  // (cta_group::2 MMAs; each CTA stages half of B). 0 forces single CTAs.
+  int pair = 1;
 };
 
 // Bytes of split workspace gemm_launch needs for M x N with `splitk` slices.

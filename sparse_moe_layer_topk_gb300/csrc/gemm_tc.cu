@@ -40,12 +40,15 @@ constexpr int MISC_BYTES = 768;  // barriers (256 B) + 128 gather row indices (5
 
 // BN: tile width (UMMA N); EW: epilogue warps (4, or 8 for heavy epilogues:
 // two warps per TMEM lane quadrant, splitting the tile's column chunks).
-template <int BN, int EW, bool CW16 = false>
+// PAIR: the CTA is one of a pair computing 256-row tiles with cta_group::2 MMAs
+// (each CTA holds its 128 rows of A and half of B's columns).
+template <int BN, int EW, bool CW16 = false, bool PAIR = false>
 struct Cfg {
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? ((EW == 8 && !CW16) ? 3 : 4)
-                                            : ((EW == 8 && !CW16) ? 5 : 6);
+  static constexpr int STAGES =
+      PAIR ? ((EW == 8 && !CW16) ? 5 : 6)
+           : ((BN == 256) ? ((EW == 8 && !CW16) ? 3 : 4) : ((EW == 8 && !CW16) ? 5 : 6));
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int THREADS = 64 + 32 * EW;
   // Per-warp output staging, a ring of slots of one chunk's output each (4 KB
@@ -102,6 +105,8 @@ struct Params {
   // (unpermuted) source tensor, loaded with TMA tile::gather4.
   const int* gather_idx;
   int gather_a, gather_b;
+  int pair;  // 1: CTA pairs (cluster of 2) own 256-row tiles (dense schedule)
+  int mt2;   // pair rows of tiles: ceil(mt / 2)
 };
 
 struct Tile {
@@ -121,7 +126,17 @@ __device__ __forceinline__ int total_tiles(const Params& p) {
   return p.total_static;
 }
 
-template <int BN>
+// A CTA (or a CTA pair) walks tiles tile_begin + i * tile_step.
+template <bool PAIR>
+__device__ __forceinline__ int tile_begin() {
+  return static_cast<int>(blockIdx.x) >> (PAIR ? 1 : 0);
+}
+template <bool PAIR>
+__device__ __forceinline__ int tile_step() {
+  return static_cast<int>(gridDim.x) >> (PAIR ? 1 : 0);
+}
+
+template <int BN, bool PAIR = false>
 __device__ __forceinline__ Tile decode(const Params& p, int t) {
   Tile ti;
   const int bn_eff = p.swiglu_b ? BN / 2 : BN;
@@ -163,12 +178,16 @@ __device__ __forceinline__ Tile decode(const Params& p, int t) {
     ti.krows = seg1 - seg0;
     ti.nk = (ti.krows + BK - 1) / BK;
   } else {
-    // split-K: the slice index is the outer tile index and takes the role of g
-    const int per = p.mt * p.nt;
+    // split-K: the slice index is the outer tile index and takes the role of g;
+    // a CTA pair's tile is two 128-row blocks, the CTA's rank picking its block
+    // (the second block of a last odd pair has no rows: rows <= 0)
+    const int mtx = PAIR ? p.mt2 : p.mt;
+    const int per = mtx * p.nt;
     ti.g = t / per;
     t -= ti.g * per;
-    ti.n_blk = t / p.mt;
-    const int m_blk = t - ti.n_blk * p.mt;
+    ti.n_blk = t / mtx;
+    int m_blk = t - ti.n_blk * mtx;
+    if (PAIR) m_blk = 2 * m_blk + static_cast<int>(cluster_ctarank());
     ti.m0 = m_blk * BM;
     ti.rows = min(BM, p.M - ti.m0);
     if (p.b_batch_mode == BATCH_FROM_N) {
@@ -200,9 +219,9 @@ __device__ __forceinline__ int4 pack_tile(const Params& p, const Tile& ti) {
 
 // The i-th tile (t = blockIdx.x + i * gridDim.x) of this CTA: from the table when
 // it holds it (the first `cap` tiles), else decoded from the schedule.
-template <int BN>
+template <int BN, bool PAIR = false>
 __device__ __forceinline__ Tile tile_of(const Params& p, const int4* ttab, int cap, int i, int t) {
-  if (p.sched == SCHED_DENSE || i >= cap) return decode<BN>(p, t);
+  if (p.sched == SCHED_DENSE || i >= cap) return decode<BN, PAIR>(p, t);
   const int4 e = ttab[i];
   const int bn_eff = p.swiglu_b ? BN / 2 : BN;
   Tile ti;
@@ -230,14 +249,16 @@ __device__ __forceinline__ Tile tile_of(const Params& p, const int4* ttab, int c
 
 // ------------------------------------------------------------------ producer
 
-template <int BN, int EW, bool CW16, bool WARP>
+template <int BN, int EW, bool CW16, bool PAIR, bool WARP>
 __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CUtensorMap* mapB,
                               const CUtensorMap* mapA2, const CUtensorMap* mapB2,
                               uint8_t* smem, uint64_t* full, uint64_t* empty, int* sidx,
                               const int4* ttab, volatile int* abort_flag) {
   // WARP: run by the whole warp (the lanes fetch gather indices and issue the
-  // gather4 copies, lane 0 the others); otherwise by lane 0 alone.
-  using C = Cfg<BN, EW, CW16>;
+  // gather4 copies, lane 0 the others); otherwise by lane 0 alone. PAIR: the
+  // CTA loads its own 128 rows of A and its half of the tile's B columns.
+  using C = Cfg<BN, EW, CW16, PAIR>;
+  const int half_n = PAIR ? static_cast<int>(cluster_ctarank()) * (BN / 2) : 0;
   const uint32_t lane = WARP ? lane_id() : 0u;
   int stage = 0;
   uint32_t phase = 0;
@@ -247,8 +268,8 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
   const bool gather_k = WARP && (p.gather_a || p.gather_b) && p.sched == SCHED_GROUPED_K;
   bool ok = true;
   int it = 0;
-  for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-    const Tile ti = tile_of<BN>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
+  for (int t = tile_begin<PAIR>(); t < total && ok; t += tile_step<PAIR>(), ++it) {
+    const Tile ti = tile_of<BN, PAIR>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
     if (gather_m) {
       // source rows of the tile's 128 A rows; rows past the expert's segment
       // repeat its last row (their results are never stored)
@@ -259,7 +280,9 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
     }
     for (int kb = 0; kb < ti.nk; ++kb) {
       int okw = 1;
-      if (lane == 0) okw = mbar_wait(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
+      // (pairs: the stage is freed by the first CTA's MMA completion, a tcgen05
+      // commit multicast to both CTAs)
+      if (lane == 0) okw = mbar_wait<PAIR>(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
       if (WARP) okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
       if (!okw) {
         if (lane == 0) raise_abort(abort_flag, p.err_flag);
@@ -294,7 +317,42 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
           tma_gather4(sB + c * CHUNK_BYTES + g * 512, mapB, &full[stage], ti.nb0 + 64 * c, gi[g]);
         }
       }
-      if (lane == 0) {
+      if (PAIR && lane == 0) {
+        // Both CTAs' copies of the stage count on the first CTA's full barrier,
+        // whose producer posts the bytes of both.
+        const uint32_t fb = half_n == 0 ? smem_u32(&full[stage])
+                                        : cluster_map(smem_u32(&full[stage]), 0);
+        if (half_n == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+        int kb_coord = k, batch = ti.batch;
+        if (p.b_batch_mode == BATCH_FROM_K) {
+          batch = k / p.k_per_batch;
+          kb_coord = k - batch * p.k_per_batch;
+        }
+        if (p.kcat > 0 && k >= p.kcat) {
+          tma_load_2d_pair(sA, mapA2, fb, k - p.kcat, ti.m0);
+          tma_load_2d_pair(sB, mapB2, fb, k - p.kcat, ti.nb0 + half_n);
+        } else {
+          if (!p.a_mn) {
+            tma_load_2d_pair(sA, mapA, fb, k, ti.m0);
+          } else if (p.a_chunked) {
+            tma_load_3d_pair(sA, mapA, fb, 0, k, ti.m0 >> 6);
+          } else {
+            tma_load_2d_pair(sA, mapA, fb, ti.m0, k);
+            tma_load_2d_pair(sA + CHUNK_BYTES, mapA, fb, ti.m0 + 64, k);
+          }
+          if (!p.b_mn) {
+            if (p.b_rank3) tma_load_3d_pair(sB, mapB, fb, kb_coord, ti.nb0 + half_n, batch);
+            else tma_load_2d_pair(sB, mapB, fb, kb_coord, ti.nb0 + half_n);
+          } else {
+            // chunked map (required for pairs): the CTA's BN/128 chunks, its half
+            // of the tile (SwiGLU pair: the gate half in CTA 0, the up half in CTA 1)
+            const int c0 =
+                (p.swiglu_b ? (half_n == 0 ? ti.nb0 : p.f + ti.nb0) : ti.nb0 + half_n) >> 6;
+            if (p.b_rank3) tma_load_4d_pair(sB, mapB, fb, 0, kb_coord, c0, batch);
+            else tma_load_3d_pair(sB, mapB, fb, 0, kb_coord, c0);
+          }
+        }
+      } else if (lane == 0) {
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
         if (p.kcat > 0 && k >= p.kcat) {
           // second K segment: [A | A2] @ [B ; B2] (both K-major, dense)
@@ -369,9 +427,11 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
       }
     }
     if (WARP) __syncwarp();
-  } else {
+  } else if (!(PAIR && half_n != 0)) {
     // Wait (bounded, ignoring the abort flag) for the copies still in flight so
-    // that none lands in shared memory after the CTA exits.
+    // that none lands in shared memory after the CTA exits. (The second CTA of
+    // a pair cannot see its copies complete: they count on the first CTA's
+    // barriers, whose producer waits for them, and the pair leaves together.)
     int s = stage;
     uint32_t ph = phase;
     volatile int never = 0;
@@ -399,7 +459,7 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   const int total = total_tiles(p);
   int it = 0;
   bool ok = true;
-  for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+  for (int t = tile_begin<false>(); t < total && ok; t += tile_step<false>(), ++it) {
     const Tile ti = tile_of<BN>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
@@ -468,6 +528,69 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   if (*abort_flag && issued_any) {
     // Let every issued MMA finish before tensor memory is released.
     if (lane == 0) mma_commit(drain);
+    __syncwarp();
+    volatile int never = 0;
+    mbar_wait(drain, 0, &never);
+  }
+}
+
+// CTA pair, first CTA: the MMA warp. A stage is full once both CTAs' copies
+// landed (both count on this CTA's full barrier); the MMAs' completion frees
+// the stage in both CTAs and, per tile, fills both CTAs' accumulators
+// (multicast commits). The accumulator buffer is free once the epilogue warps
+// of both CTAs released it (tempty, 2 * EW arrivals).
+template <int BN, int EW, bool CW16>
+__device__ void mma_loop_pair(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* tfull, uint64_t* tempty, uint64_t* drain,
+                              uint32_t tmem_base, volatile int* abort_flag) {
+  using C = Cfg<BN, EW, CW16, true>;
+  const uint32_t lane = lane_id();
+  const uint32_t idesc = make_idesc_bf16(2 * BM, BN, p.a_mn, p.b_mn);
+  const uint32_t a_lbo = p.a_mn ? CHUNK_BYTES : 16, b_lbo = p.b_mn ? CHUNK_BYTES : 16;
+  const uint32_t a_kstep = p.a_mn ? 2048 : 32, b_kstep = p.b_mn ? 2048 : 32;
+  int stage = 0;
+  uint32_t phase = 0;
+  bool issued_any = false;
+  const int total = total_tiles(p);
+  int it = 0;
+  bool ok = true;
+  for (int t = tile_begin<true>(); t < total && ok; t += tile_step<true>(), ++it) {
+    const Tile ti = decode<BN, true>(p, t);
+    const int buf = it & 1;
+    const uint32_t use = static_cast<uint32_t>(it >> 1);
+    if (!mbar_wait<true>(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
+      raise_abort(abort_flag, p.err_flag);
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+    for (int kb = 0; kb < ti.nk; ++kb) {
+      if (!mbar_wait(&full[stage], phase, abort_flag)) {
+        raise_abort(abort_flag, p.err_flag);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES), b0 = a0 + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = make_sdesc(a0 + kk * a_kstep, a_lbo, 1024);
+          const uint64_t bd = make_sdesc(b0 + kk * b_kstep, b_lbo, 1024);
+          mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        mma_commit_pair(&empty[stage], 0x3);
+      }
+      issued_any = true;
+      __syncwarp();
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+    }
+    if (!ok) break;
+    if (lane == 0) mma_commit_pair(&tfull[buf], 0x3);  // nk > 0 on the dense schedule
+    __syncwarp();
+  }
+  if (*abort_flag && issued_any) {
+    // Let every issued MMA finish before tensor memory is released.
+    if (lane == 0) mma_commit_pair(drain, 0x1);
     __syncwarp();
     volatile int never = 0;
     mbar_wait(drain, 0, &never);
@@ -567,7 +690,7 @@ struct StoreMaps {
   int c0_rank3;
 };
 
-template <int BN, int EW, bool CW16>
+template <int BN, int EW, bool CW16, bool PAIR>
 __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* staging,
                               uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base,
                               const int4* ttab, volatile int* abort_flag) {
@@ -606,11 +729,11 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
     __syncwarp();
   };
   int it = 0;
-  for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-    const Tile ti = tile_of<BN>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
+  for (int t = tile_begin<PAIR>(); t < total; t += tile_step<PAIR>(), ++it) {
+    const Tile ti = tile_of<BN, PAIR>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
-    if (!mbar_wait(&tfull[buf], use & 1u, abort_flag)) {
+    if (!mbar_wait<PAIR>(&tfull[buf], use & 1u, abort_flag)) {
       raise_abort(abort_flag, p.err_flag);
       break;
     }
@@ -875,23 +998,25 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
         } else {
         const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
         float dot = 0.0f;
-        // g and u of the next chunk are loaded one chunk ahead, h of the current
-        // chunk at its start (it is needed last); results go to the staging
-        // blocks 8 columns at a time to keep the register footprint small.
-        uint4 Gn[4], Un[4];
-        auto load_gu = [&](int n, uint4* G, uint4* U) {
+        // g, u and h of the warp's next chunk are loaded one chunk ahead; results
+        // go to the staging blocks 8 columns at a time to keep the register
+        // footprint small.
+        uint4 Gn[4], Un[4], Hn[4];
+        auto load_guh = [&](int n, uint4* G, uint4* U, uint4* H) {
           const int s = n / p.f;
           const bf16* gsrc = p.gu + grow * p.ldgu + s * 2 * p.f + (n - s * p.f);
+          const bf16* hsrc = p.h + grow * p.ldh + n;
 #pragma unroll
           for (int vv = 0; vv < 4; ++vv) {
             G[vv] = *reinterpret_cast<const uint4*>(gsrc + vv * 8);
             U[vv] = *reinterpret_cast<const uint4*>(gsrc + p.f + vv * 8);
+            H[vv] = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
           }
         };
         const uint4 z4 = make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
-        if (row_ok && ti.nb0 + grp * 32 < p.N) load_gu(ti.nb0 + grp * 32, Gn, Un);
+        for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; Hn[vv] = z4; }
+        if (row_ok && ti.nb0 + grp * 32 < p.N) load_guh(ti.nb0 + grp * 32, Gn, Un, Hn);
         const int sw = (lane >> 1) & 3;  // 64-byte swizzle of this lane's staging row
 #pragma unroll 1
         for (int c = grp; c < BN / 32; c += NG) {
@@ -899,13 +1024,8 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           if (n >= p.N) break;
           uint4 Gc[4], Uc[4], Hc[4];
 #pragma unroll
-          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; Hc[vv] = z4; }
-          if (row_ok) {
-            const bf16* hsrc = p.h + grow * p.ldh + n;
-#pragma unroll
-            for (int vv = 0; vv < 4; ++vv) Hc[vv] = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
-            if (c + NG < BN / 32 && n + 32 * NG < p.N) load_gu(n + 32 * NG, Gn, Un);
-          }
+          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; Hc[vv] = Hn[vv]; }
+          if (row_ok && c + NG < BN / 32 && n + 32 * NG < p.N) load_guh(n + 32 * NG, Gn, Un, Hn);
           float a[32];
           ld_chunk(trow + c * 32, a);
           const int s = n / p.f;
@@ -969,13 +1089,19 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
       }
     }
     tc_fence_before();
-    mbar_arrive(&tempty[buf]);
+    if (PAIR) {
+      // one arrival per warp on the pair's first CTA (it issues the MMAs)
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&tempty[buf]), 0));
+    } else {
+      mbar_arrive(&tempty[buf]);
+    }
   }
   if (lane == 0) bulk_wait_all();
   __syncwarp();
 }
 
-template <int BN, int EW, bool CW16>
+template <int BN, int EW, bool CW16, bool PAIR>
 __global__ void __launch_bounds__(64 + 32 * EW, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
@@ -983,7 +1109,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
                    const __grid_constant__ CUtensorMap mapC1,
                    const __grid_constant__ CUtensorMap mapA2,
                    const __grid_constant__ CUtensorMap mapB2, const Params p) {
-  using C = Cfg<BN, EW, CW16>;
+  using C = Cfg<BN, EW, CW16, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1016,7 +1142,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 32 * EW);
+      mbar_init(&tempty[b], PAIR ? 2 * EW : 32 * EW);  // pairs: one arrival per warp of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -1025,34 +1151,50 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     tma_prefetch_desc(&mapB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR) cluster_sync_all();  // the other CTA's barriers are initialised too
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // Gathering launches run the producer on the whole warp (the lanes fetch
     // indices and issue gather4 copies); the others on lane 0 alone.
-    if (p.gather_a || p.gather_b)
-      producer_loop<BN, EW, CW16, true>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty, sidx,
-                                        ttab, abort_flag);
+    if (!PAIR && (p.gather_a || p.gather_b))
+      producer_loop<BN, EW, CW16, PAIR, true>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty,
+                                              sidx, ttab, abort_flag);
     else if (lane_id() == 0)
-      producer_loop<BN, EW, CW16, false>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty, sidx,
-                                         ttab, abort_flag);
+      producer_loop<BN, EW, CW16, PAIR, false>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty,
+                                               sidx, ttab, abort_flag);
   } else if (warp == 1) {
-    mma_loop<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base, ttab, abort_flag);
+    if constexpr (!PAIR) {
+      mma_loop<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base, ttab,
+                             abort_flag);
+    } else {
+      if (cluster_ctarank() == 0)  // the second CTA's MMA warp has nothing to do
+        mma_loop_pair<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base,
+                                    abort_flag);
+    }
   } else {
     const StoreMaps sm{&mapC0, &mapC1, p.c0_rank3};
-    epilogue_loop<BN, EW, CW16>(p, sm, staging, tfull, tempty, tmem_base, ttab, abort_flag);
+    epilogue_loop<BN, EW, CW16, PAIR>(p, sm, staging, tfull, tempty, tmem_base, ttab, abort_flag);
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR) cluster_sync_all();  // no CTA frees tensor memory the pair's MMAs may still use
+  else __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -1132,10 +1274,11 @@ bool make_store_map(CUtensorMap* map, void* ptr, bool f32, bool rank3, long long
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int EW, bool CW16>
+template <int BN, int EW, bool CW16, bool PAIR>
 int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
-  using C = Cfg<BN, EW, CW16>;
+  using C = Cfg<BN, EW, CW16, PAIR>;
   Params p{};
+  p.pair = PAIR ? 1 : 0;
   p.sched = L.sched;
   p.M = L.M;
   p.N = L.N;
@@ -1161,7 +1304,8 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
     p.splitk = L.splitk > 1 ? L.splitk : 1;
     p.kslice = ((L.K + p.splitk - 1) / p.splitk + BK - 1) / BK * BK;
     p.splitk = (L.K + p.kslice - 1) / p.kslice;
-    p.total_static = p.mt * p.nt * p.splitk;
+    p.mt2 = (p.mt + 1) / 2;
+    p.total_static = (PAIR ? p.mt2 : p.mt) * p.nt * p.splitk;
     upper = p.total_static;
   } else if (L.sched == SCHED_GROUPED_K) {
     p.total_static = L.G * p.mt * p.nt;
@@ -1213,7 +1357,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
     if (L.sched != SCHED_DENSE || L.a_mn || L.b_mn || L.b_batch_mode != BATCH_NONE ||
         L.kcat % BK != 0 || L.splitk > 1 || L.gather_a || L.gather_b)
       return MOE_ERR_UNSUPPORTED;
-    if (!make_map(&mapA2, L.A2, BM, false) || !make_map(&mapB2, L.B2, BN, false))
+    if (!make_map(&mapA2, L.A2, BM, false) || !make_map(&mapB2, L.B2, PAIR ? BN / 2 : BN, false))
       return MOE_ERR_ARG;
     p.kcat = L.kcat;
   }
@@ -1223,11 +1367,14 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   // (the chunk coordinate is m0 / 64: grouped-M row starts are not 64-aligned)
   p.a_chunked = L.a_mn && !L.gather_a && L.sched != SCHED_GROUPED_M &&
                 make_map_chunked(&mapA, L.A, BM / 64, false);
+  // (a CTA of a pair loads half of the tile's B columns: BN/128 chunks)
   p.b_chunked = L.b_mn && !L.gather_b &&
-                make_map_chunked(&mapB, L.B, L.swiglu_b ? BN / 128 : BN / 64, b3);
+                make_map_chunked(&mapB, L.B, (PAIR || L.swiglu_b) ? BN / 128 : BN / 64, b3);
+  if (PAIR && L.b_mn && !p.b_chunked) return MOE_ERR_UNSUPPORTED;
   if (!p.a_chunked && !make_map(&mapA, L.A, L.gather_a ? 1 : (L.a_mn ? 64 : BM), false))
     return MOE_ERR_ARG;
-  if (!p.b_chunked && !make_map(&mapB, L.B, L.gather_b ? 1 : (L.b_mn ? 64 : BN), b3))
+  if (!p.b_chunked &&
+      !make_map(&mapB, L.B, L.gather_b ? 1 : (L.b_mn ? 64 : (PAIR ? BN / 2 : BN)), b3))
     return MOE_ERR_ARG;
   // output (store) maps
   const long long rows_out = (L.sched == SCHED_GROUPED_M) ? L.R_cap : L.M;
@@ -1271,7 +1418,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EW, CW16>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EW, CW16, PAIR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) {
@@ -1280,13 +1427,34 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
     }
     attr_set[dev] = true;
   }
-  const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
-  {
+  cudaError_t e;
+  if (PAIR) {
+    // clusters of two CTAs, one pair tile each at a time
+    const long long pairs = num_sms() / 2;
+    const int grid = 2 * static_cast<int>(upper < pairs ? upper : pairs);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     LaunchTimer lt(L.name, stream);
-    gemm_tc_kernel<BN, EW, CW16><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EW, CW16, PAIR>, mapA, mapB, mapC0, mapC1,
+                           mapA2, mapB2, p);
+  } else {
+    const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
+    LaunchTimer lt(L.name, stream);
+    gemm_tc_kernel<BN, EW, CW16, PAIR><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
         mapA, mapB, mapC0, mapC1, mapA2, mapB2, p);
+    e = cudaSuccess;
   }
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return MOE_ERR_CUDA;
@@ -1344,13 +1512,23 @@ int gemm_launch(const GemmLaunch& L, cudaStream_t stream) {
   // The SwiGLU forward epilogue works on 16-column chunks (smaller staging, one
   // more pipeline stage); its backward on 32-column chunks.
   const bool cw16 = L.epi == EPI_SWIGLU;
+  // CTA pairs (256-row tiles, cta_group::2 MMAs, half of B per CTA) for the dense
+  // schedule with 256-wide tiles and at least two row blocks
+  const bool pair = L.pair && L.BN == 256 && L.sched == SCHED_DENSE && L.K > 0 && L.M > BM &&
+                    !L.gather_a && !L.gather_b;
   int st;
-  if (L.BN == 256)
-    st = ew == 4 ? launch_bn<256, 4, false>(L, stream)
-                 : (cw16 ? launch_bn<256, 8, true>(L, stream) : launch_bn<256, 8, false>(L, stream));
+  if (L.BN == 256 && pair)
+    st = ew == 4 ? launch_bn<256, 4, false, true>(L, stream)
+                 : (cw16 ? launch_bn<256, 8, true, true>(L, stream)
+                         : launch_bn<256, 8, false, true>(L, stream));
+  else if (L.BN == 256)
+    st = ew == 4 ? launch_bn<256, 4, false, false>(L, stream)
+                 : (cw16 ? launch_bn<256, 8, true, false>(L, stream)
+                         : launch_bn<256, 8, false, false>(L, stream));
   else if (L.BN == 128)
-    st = ew == 4 ? launch_bn<128, 4, false>(L, stream)
-                 : (cw16 ? launch_bn<128, 8, true>(L, stream) : launch_bn<128, 8, false>(L, stream));
+    st = ew == 4 ? launch_bn<128, 4, false, false>(L, stream)
+                 : (cw16 ? launch_bn<128, 8, true, false>(L, stream)
+                         : launch_bn<128, 8, false, false>(L, stream));
   else
     return MOE_ERR_UNSUPPORTED;
   if (st != MOE_OK || L.splitk <= 1) return st;

@@ -27,11 +27,13 @@ def _bf16(seed, *shape, std=1.0):
 # ---------------------------------------------------------------- GEMM engine
 
 @pytest.mark.parametrize("M_,K,N", [(300, 256, 192), (128, 64, 64), (1000, 512, 1024), (5, 128, 256),
-                                    (700, 1024, 512), (2000, 1024, 768)])
+                                    (700, 1024, 512), (2000, 1024, 768), (1100, 256, 512),
+                                    (129, 384, 256)])
 def test_latent_proj_and_bwd(M_, K, N):
     """Every operand layout of the tcgen05 engine: A K-major / B MN-major
     (forward), B K-major (dgrad), A and B MN-major (wgrad); ragged M and an
-    N tail narrower than the tile."""
+    N tail narrower than the tile; 256-wide tiles run on CTA pairs, including
+    an odd number of 128-row blocks (the last pair's second CTA has no rows)."""
     x = _bf16(1, M_, K)
     W = _bf16(2, K, N, std=0.02)  # |out| ~ 1: bf16 output rounding stays below 2e-2
     dout = _bf16(3, M_, N)
