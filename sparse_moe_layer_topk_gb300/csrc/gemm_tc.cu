@@ -998,25 +998,23 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
         } else {
         const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
         float dot = 0.0f;
-        // g, u and h of the warp's next chunk are loaded one chunk ahead; results
-        // go to the staging blocks 8 columns at a time to keep the register
-        // footprint small.
-        uint4 Gn[4], Un[4], Hn[4];
-        auto load_guh = [&](int n, uint4* G, uint4* U, uint4* H) {
+        // g and u of the next chunk are loaded one chunk ahead, h of the current
+        // chunk at its start (it is needed last); results go to the staging
+        // blocks 8 columns at a time to keep the register footprint small.
+        uint4 Gn[4], Un[4];
+        auto load_gu = [&](int n, uint4* G, uint4* U) {
           const int s = n / p.f;
           const bf16* gsrc = p.gu + grow * p.ldgu + s * 2 * p.f + (n - s * p.f);
-          const bf16* hsrc = p.h + grow * p.ldh + n;
 #pragma unroll
           for (int vv = 0; vv < 4; ++vv) {
             G[vv] = *reinterpret_cast<const uint4*>(gsrc + vv * 8);
             U[vv] = *reinterpret_cast<const uint4*>(gsrc + p.f + vv * 8);
-            H[vv] = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
           }
         };
         const uint4 z4 = make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; Hn[vv] = z4; }
-        if (row_ok && ti.nb0 + grp * 32 < p.N) load_guh(ti.nb0 + grp * 32, Gn, Un, Hn);
+        for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
+        if (row_ok && ti.nb0 + grp * 32 < p.N) load_gu(ti.nb0 + grp * 32, Gn, Un);
         const int sw = (lane >> 1) & 3;  // 64-byte swizzle of this lane's staging row
 #pragma unroll 1
         for (int c = grp; c < BN / 32; c += NG) {
@@ -1024,8 +1022,13 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           if (n >= p.N) break;
           uint4 Gc[4], Uc[4], Hc[4];
 #pragma unroll
-          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; Hc[vv] = Hn[vv]; }
-          if (row_ok && c + NG < BN / 32 && n + 32 * NG < p.N) load_guh(n + 32 * NG, Gn, Un, Hn);
+          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; Hc[vv] = z4; }
+          if (row_ok) {
+            const bf16* hsrc = p.h + grow * p.ldh + n;
+#pragma unroll
+            for (int vv = 0; vv < 4; ++vv) Hc[vv] = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
+            if (c + NG < BN / 32 && n + 32 * NG < p.N) load_gu(n + 32 * NG, Gn, Un);
+          }
           float a[32];
           ld_chunk(trow + c * 32, a);
           const int s = n / p.f;
