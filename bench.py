@@ -280,8 +280,8 @@ def _event_time(fn, steps, warmup, stream):
 
 
 def secondary_workloads(steps, warmup, tc_peak):
-    """Forward-only tokens/s at T=4096 (uniform and Zipf-skewed routing) and the
-    expert-parallel rank workload (grouped SwiGLU GEMMs + return to arrival
+    """Forward-only tokens/s at T=4096 (uniform and Zipf-skewed routing), the
+    bench step with bf16 weight gradients, and the expert-parallel rank workload (grouped SwiGLU GEMMs + return to arrival
     order, 14 experts x 65536 rows), each timed with CUDA events after warm-up.
     Returns a dict for the JSON line."""
     import numpy as np
@@ -322,6 +322,18 @@ def secondary_workloads(steps, warmup, tc_peak):
             _event_time(bucketed, steps, warmup, stream), 4)
         del layer, inp, x
         torch.cuda.empty_cache()
+    # the bench step with bf16 weight gradients (halves the expert gradient writes)
+    cfg = I.CONFIGS[4]
+    inp = I.make_layer_inputs(cfg)
+    layer = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_BF16)
+    x, g = inp["x"].cuda(), inp["g"].cuda()
+    layer.step(x, g)
+    graph = layer.capture_step(x, g)
+    ms = _event_time(graph.replay, steps, warmup, stream)
+    out[cfg.name + "_bf16_wgrad"] = {"ms_per_step": round(ms, 4),
+                                      "tokens_per_s": cfg.T / (ms / 1000.0)}
+    del graph, layer, inp, x, g
+    torch.cuda.empty_cache()
     ep = I.make_ep_rank_inputs()
     c = ep["cfg"]
     counts = ep["counts"].numpy().astype(np.int64)
