@@ -7,8 +7,9 @@
 //                         shared memory -> per-chunk expert histogram.
 //   scan_kernel           one CTA: per-expert prefix over chunks, exclusive
 //                         scan over experts (offsets), 128-row tile schedule.
-//   maps_kernel           slot = chunk base + popcount of the expert's token
-//                         bits below this token: stable, atomics-free ranks.
+//   maps_kernel           slot = expert offset + chunk prefix + popcount of the
+//                         expert's token bits below this token: stable,
+//                         atomics-free ranks.
 //   gather_rows_kernel    dst[r] = src[index[r]] with 16-byte vectors (permute,
 //                         combine backward).
 //   gather_sum_kernel     out[t] = sum_j src[slot[t][j]] (+ add[t]) in fp32
@@ -209,10 +210,17 @@ __global__ void __launch_bounds__(1024) scan_kernel(int* __restrict__ hist, int 
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = hist[static_cast<size_t>(c) * E + e];
-      hist[static_cast<size_t>(c) * E + e] = cnt;
-      cnt += v;
+    // sixteen chunks' counts loaded together, then the running prefix stored
+    for (int c0 = 0; c0 < nchunks; c0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[i] = (c0 + i < nchunks) ? hist[static_cast<size_t>(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (c0 + i < nchunks) hist[static_cast<size_t>(c0 + i) * E + e] = cnt;
+        cnt += v[i];
+      }
     }
     counts[e] = cnt;
   }
@@ -220,10 +228,9 @@ __global__ void __launch_bounds__(1024) scan_kernel(int* __restrict__ hist, int 
   int rows_total = 0, tiles_total = 0;
   const int off = block_inclusive_scan(cnt, warp_sums, &rows_total) - cnt;
   const int ts = block_inclusive_scan(tiles, warp_sums, &tiles_total) - tiles;
-  if (e < E) {
+  if (e < E) {  // (the maps kernel adds offsets[e] to the per-chunk prefixes)
     offsets[e] = off;
     tile_sched[e] = ts;
-    for (int c = 0; c < nchunks; ++c) hist[static_cast<size_t>(c) * E + e] += off;
   }
   if (e == 0) {
     offsets[E] = rows_total;
@@ -235,6 +242,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int* __restrict__ hist, int 
 
 __global__ void __launch_bounds__(kChunk) maps_kernel(const int* __restrict__ idx, int T, int E,
                                                       int k, const int* __restrict__ base,
+                                                      const int* __restrict__ offsets,
                                                       const float* __restrict__ topk_w,
                                                       int* __restrict__ slot_of,
                                                       int* __restrict__ token_of,
@@ -254,7 +262,7 @@ __global__ void __launch_bounds__(kChunk) maps_kernel(const int* __restrict__ id
     }
     int rank = __popc(bits[e * 8 + word] & below);
     for (int wd = 0; wd < word; ++wd) rank += __popc(bits[e * 8 + wd]);
-    const int slot = __ldg(base + static_cast<size_t>(blockIdx.x) * E + e) + rank;
+    const int slot = __ldg(base + static_cast<size_t>(blockIdx.x) * E + e) + __ldg(offsets + e) + rank;
     slot_of[o] = slot;
     token_of[slot] = t;
     if (row_w) row_w[slot] = __ldg(topk_w + o);
@@ -560,7 +568,8 @@ cudaError_t launch_permute_maps(const int* idx, const float* topk_w, int T, int 
   }
   {
     LaunchTimer lt("permute_maps", st);
-    maps_kernel<<<nch, kChunk, sm, st>>>(idx, T, E, k, hist_ws, topk_w, slot_of, token_of, row_w);
+    maps_kernel<<<nch, kChunk, sm, st>>>(idx, T, E, k, hist_ws, offsets, topk_w, slot_of, token_of,
+                                         row_w);
   }
   return cudaGetLastError();
 }
