@@ -263,8 +263,10 @@ def test_grouped_swiglu_fwd_bwd(counts, l, f):
 
 
 @pytest.mark.parametrize("T,l,f,S", [(256, 128, 64, 1), (1000, 1024, 512, 2), (77, 256, 128, 3),
-                                     (4096, 1024, 512, 2)])
+                                     (4096, 1024, 512, 2), (1100, 512, 256, 2)])
 def test_shared_swiglu_fwd_bwd(T, l, f, S):
+    """Dense SwiGLU experts on all tokens (CTA pairs for the 256-wide tiles; T=1100
+    has an odd number of 128-row blocks)."""
     z = _bf16(30, T, l)
     W13 = _bf16(31, S, l, 2 * f, std=0.02)
     W2 = _bf16(32, S, f, l, std=0.02)
@@ -471,9 +473,11 @@ def test_bucket_order_and_ordered_grouped_gemm(skew):
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
-def test_route_topk_bwd_fused_down_projection_dgrad():
-    """dx = dz W_dn^T + dL Wr^T as one K-concatenated GEMM (K = l + E)."""
-    T, d, E, k, l = 500, 512, 128, 4, 256
+@pytest.mark.parametrize("T", [500, 300])
+def test_route_topk_bwd_fused_down_projection_dgrad(T):
+    """dx = dz W_dn^T + dL Wr^T as one K-concatenated GEMM (K = l + E), on CTA
+    pairs; T=300 leaves the last pair's second CTA without rows."""
+    d, E, k, l = 512, 128, 4, 256
     x = _bf16(90, T, d)
     Wr = _bf16(91, d, E, std=0.02)
     W_dn = _bf16(92, d, l, std=0.02)
