@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fused-gather", action="store_true",
+                    help="the grouped GEMMs gather their permuted rows themselves")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of CUDA-graph replays of the step")
     ap.add_argument("--no-secondary", action="store_true",
@@ -394,7 +396,7 @@ def run_ours(args):
     T = cfg.T
     inp = I.make_layer_inputs(cfg)
     wdt = M.MOE_DTYPE_F32 if args.wgrad == "f32" else M.MOE_DTYPE_BF16
-    layer = LatentMoELayer(weights_to_device(inp), T, cfg.k, wdt)
+    layer = LatentMoELayer(weights_to_device(inp), T, cfg.k, wdt, fused_gather=args.fused_gather)
     x = inp["x"].cuda()
     g = inp["g"].cuda()
     stream = torch.cuda.current_stream()
