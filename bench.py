@@ -70,6 +70,24 @@ def workload(args):
     return cfg
 
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time (ms): every rank's timed region covers the same
+    number of steps, so the job finishes with the slowest one."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, T, steps, ms):
+    """Whole-job throughput: every rank processes T tokens per step (replicas,
+    weak scaling) in the slowest rank's time."""
+    return world * T * steps / (ms / 1000.0)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -441,11 +459,7 @@ def run_ours(args):
         barrier()
         M.moe_timing_enable(False)
         rep = M.moe_timing_report()
-        t_ms = ev0.elapsed_time(ev1)
-        if world > 1:
-            t = torch.tensor([t_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_ms = float(t.item())
+        t_ms = max_over_ranks(ev0.elapsed_time(ev1), world, "cuda")
         return t_ms, rep
 
     clocks.start()
@@ -457,7 +471,7 @@ def run_ours(args):
         ms = ms_eager
     clk = clocks.stop()
     timing_desc = "CUDA-graph replays of the step" if graph is not None else "eager launches"
-    value = world * T * args.steps / (ms / 1000.0)
+    value = job_tokens_per_s(world, T, args.steps, ms)
     launches = sum(c for c, _ in per_kernel.values())  # the same kernels, once per step
 
     # ---- end to end: pinned host inputs in, input gradient out, every step
@@ -480,12 +494,8 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * T * args.steps / (ems / 1000.0), "unit": "tokens/s",
+        ems = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
+        e2e = {"value": job_tokens_per_s(world, T, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": int(xh.numel() * 2 + gh.numel() * 2),
                "d2h_bytes_per_step": int(dxh.numel() * 2)}
 
