@@ -753,6 +753,10 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
   MOE_REQUIRE(!(dx_accum && !Wr) && !(dWr && !x), MOE_ERR_ARG);
   MOE_REQUIRE(!dx_accum || (al16(dx_accum) && al16(Wr)), MOE_ERR_ALIGN);
   MOE_REQUIRE(!dWr || (al16(dWr) && al16(x)), MOE_ERR_ALIGN);
+  if (dx_accum && dz) {  // the fused input gradient dx = dz W_dn^T + dL Wr^T
+    MOE_REQUIRE(W_dn != nullptr && l > 0, MOE_ERR_ARG);
+    MOE_REQUIRE(l % 64 == 0 && al16(dz) && al16(W_dn), MOE_ERR_ALIGN);
+  }
   MOE_REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_ROUTE_TOPK_BWD, T, d, 0, E, k, 0, 0),
               MOE_ERR_WORKSPACE);
   cudaStream_t st = S(stream);
@@ -771,8 +775,6 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
   }
   if (dx_accum && dz) {
     // dx = dz @ W_dn^T + dL @ Wr^T as one GEMM over K = l + E (overwrites dx)
-    MOE_REQUIRE(W_dn != nullptr && l > 0, MOE_ERR_ARG);
-    MOE_REQUIRE(l % 64 == 0 && al16(dz) && al16(W_dn), MOE_ERR_ALIGN);
     GemmLaunch L;
     L.name = "down_proj_router_dgrad";
     L.BN = pick_bn(d);

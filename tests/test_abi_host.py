@@ -75,3 +75,9 @@ def test_argument_errors_before_any_cuda_call(lib):
                                       P, 1 << 30, None) == M.MOE_ERR_UNSUPPORTED
     # bad wgrad dtype
     assert lib.moe_latent_proj_bwd(P, P, P, 4, 64, 64, None, P, 7, None) == M.MOE_ERR_ARG
+    # the fused input gradient of the router backward: latent width not a
+    # multiple of 64, or no W_dn, is refused before anything is enqueued
+    assert lib.moe_route_topk_bwd(P, P, P, P, P, P, P, 64, 64, 64, 4, None, P, None, 0, None, None,
+                                  None, 0.0, P, P, 96, P, 1 << 30, None, None) == M.MOE_ERR_ALIGN
+    assert lib.moe_route_topk_bwd(P, P, P, P, P, P, P, 64, 64, 64, 4, None, P, None, 0, None, None,
+                                  None, 0.0, P, None, 128, P, 1 << 30, None, None) == M.MOE_ERR_ARG
