@@ -271,15 +271,15 @@ int moe_latent_proj_bwd(const uint16_t* dout, const uint16_t* in, const uint16_t
   MOE_REQUIRE(M >= 0 && K > 0 && N > 0, MOE_ERR_ARG);
   MOE_REQUIRE(K % 64 == 0 && N % 64 == 0, MOE_ERR_ALIGN);
   MOE_REQUIRE(wgrad_dtype == MOE_DTYPE_F32 || wgrad_dtype == MOE_DTYPE_BF16, MOE_ERR_ARG);
+  MOE_REQUIRE(!din || W != nullptr, MOE_ERR_ARG);
+  MOE_REQUIRE(!din || (al16(dout) && al16(W) && al16(din)), MOE_ERR_ALIGN);
+  MOE_REQUIRE(!dW || in != nullptr, MOE_ERR_ARG);
+  MOE_REQUIRE(!dW || (al16(dout) && al16(in) && al16(dW)), MOE_ERR_ALIGN);
   cudaStream_t st = S(stream);
   if (din) {
-    MOE_REQUIRE(W != nullptr, MOE_ERR_ARG);
-    MOE_REQUIRE(al16(dout) && al16(W) && al16(din), MOE_ERR_ALIGN);
     if (M > 0) MOE_CHECK(dense_gemm("latent_proj_dgrad", dout, N, 0, W, N, 0, M, K, N, din, K, 1, 0, st));
   }
   if (dW) {
-    MOE_REQUIRE(in != nullptr, MOE_ERR_ARG);
-    MOE_REQUIRE(al16(dout) && al16(in) && al16(dW), MOE_ERR_ALIGN);
     if (M == 0) {
       const size_t bytes = static_cast<size_t>(K) * N * (wgrad_dtype == MOE_DTYPE_F32 ? 4 : 2);
       return cuda_status(cudaMemsetAsync(dW, 0, bytes, st));
@@ -753,6 +753,7 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
   MOE_REQUIRE(!(dx_accum && !Wr) && !(dWr && !x), MOE_ERR_ARG);
   MOE_REQUIRE(!dx_accum || (al16(dx_accum) && al16(Wr)), MOE_ERR_ALIGN);
   MOE_REQUIRE(!dWr || (al16(dWr) && al16(x)), MOE_ERR_ALIGN);
+  MOE_REQUIRE(!aux_logits || aux_p_mean != nullptr, MOE_ERR_ARG);
   if (dx_accum && dz) {  // the fused input gradient dx = dz W_dn^T + dL Wr^T
     MOE_REQUIRE(W_dn != nullptr && l > 0, MOE_ERR_ARG);
     MOE_REQUIRE(l % 64 == 0 && al16(dz) && al16(W_dn), MOE_ERR_ALIGN);
@@ -770,7 +771,6 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
   MOE_CHECK(cuda_status(launch_router_bwd(d_row_w, slot_of, topk_idx, topk_w, topk_s, T, E, k,
                                           d_topk_w, dL, err_flag, st)));
   if (aux_logits) {
-    MOE_REQUIRE(aux_p_mean != nullptr, MOE_ERR_ARG);
     MOE_CHECK(cuda_status(launch_aux_bwd(aux_logits, aux_bias, aux_p_mean, T, E, aux_scale, dL, st)));
   }
   if (dx_accum && dz) {

@@ -81,3 +81,9 @@ def test_argument_errors_before_any_cuda_call(lib):
                                   None, 0.0, P, P, 96, P, 1 << 30, None, None) == M.MOE_ERR_ALIGN
     assert lib.moe_route_topk_bwd(P, P, P, P, P, P, P, 64, 64, 64, 4, None, P, None, 0, None, None,
                                   None, 0.0, P, None, 128, P, 1 << 30, None, None) == M.MOE_ERR_ARG
+    # the weight-gradient half of the projection backward is checked before the
+    # input-gradient GEMM is enqueued
+    assert lib.moe_latent_proj_bwd(P, None, P, 4, 64, 64, P, P, 0, None) == M.MOE_ERR_ARG
+    # an auxiliary-loss gradient needs the batch's mean routing distribution
+    assert lib.moe_route_topk_bwd(P, P, P, P, P, P, P, 64, 64, 64, 4, None, None, None, 0, P, None,
+                                  None, 1.0, None, None, 0, P, 1 << 30, None, None) == M.MOE_ERR_ARG
