@@ -729,6 +729,10 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
     __syncwarp();
   };
   int it = 0;
+  // SwiGLU backward: g and u of the warp's first chunk of a tile, loaded during
+  // the last chunk of the tile before (they are inputs, not accumulator data)
+  uint4 Gn[4], Un[4];
+  bool gu_ready = false;
   for (int t = tile_begin<PAIR>(); t < total; t += tile_step<PAIR>(), ++it) {
     const Tile ti = tile_of<BN, PAIR>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
     const int buf = it & 1;
@@ -998,13 +1002,12 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
         } else {
         const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
         float dot = 0.0f;
-        // g and u of the next chunk are loaded one chunk ahead, h of the current
-        // chunk at its start (it is needed last); results go to the staging
-        // blocks 8 columns at a time to keep the register footprint small.
-        uint4 Gn[4], Un[4];
-        auto load_gu = [&](int n, uint4* G, uint4* U) {
+        // g and u of the next chunk are loaded one chunk ahead (across tiles too),
+        // h of the current chunk at its start (it is needed last); results go to
+        // the staging blocks 8 columns at a time to keep the register footprint small.
+        auto load_gu = [&](long long row, int n, uint4* G, uint4* U) {
           const int s = n / p.f;
-          const bf16* gsrc = p.gu + grow * p.ldgu + s * 2 * p.f + (n - s * p.f);
+          const bf16* gsrc = p.gu + row * p.ldgu + s * 2 * p.f + (n - s * p.f);
 #pragma unroll
           for (int vv = 0; vv < 4; ++vv) {
             G[vv] = *reinterpret_cast<const uint4*>(gsrc + vv * 8);
@@ -1012,9 +1015,12 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           }
         };
         const uint4 z4 = make_uint4(0, 0, 0, 0);
+        if (!gu_ready) {
 #pragma unroll
-        for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
-        if (row_ok && ti.nb0 + grp * 32 < p.N) load_gu(ti.nb0 + grp * 32, Gn, Un);
+          for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
+          if (row_ok && ti.nb0 + grp * 32 < p.N) load_gu(grow, ti.nb0 + grp * 32, Gn, Un);
+        }
+        gu_ready = false;
         const int sw = (lane >> 1) & 3;  // 64-byte swizzle of this lane's staging row
 #pragma unroll 1
         for (int c = grp; c < BN / 32; c += NG) {
@@ -1022,12 +1028,28 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           if (n >= p.N) break;
           uint4 Gc[4], Uc[4], Hc[4];
 #pragma unroll
-          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; Hc[vv] = z4; }
+          for (int vv = 0; vv < 4; ++vv) Hc[vv] = z4;
           if (row_ok) {
             const bf16* hsrc = p.h + grow * p.ldh + n;
 #pragma unroll
             for (int vv = 0; vv < 4; ++vv) Hc[vv] = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
-            if (c + NG < BN / 32 && n + 32 * NG < p.N) load_gu(n + 32 * NG, Gn, Un);
+          }
+#pragma unroll
+          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; }
+          const bool more = c + NG < BN / 32 && n + 32 * NG < p.N;
+          if (more) {
+            if (row_ok) load_gu(grow, n + 32 * NG, Gn, Un);
+          } else if (t + tile_step<PAIR>() < total) {
+            // the warp's last chunk of this tile: fetch its first chunk of the next one
+            const Tile nt = tile_of<BN, PAIR>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it + 1,
+                                              t + tile_step<PAIR>());
+            if (nt.rows - q * 32 > 0) {  // the next tile's epilogue runs for this warp
+#pragma unroll
+              for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
+              if (r_loc < nt.rows && nt.nb0 + grp * 32 < p.N)
+                load_gu(static_cast<long long>(nt.m0) + r_loc, nt.nb0 + grp * 32, Gn, Un);
+              gu_ready = true;
+            }
           }
           float a[32];
           ld_chunk(trow + c * 32, a);
