@@ -3,8 +3,9 @@
 //   topk_sigmoid_kernel   warp per token: top-k of (logit + bias) by warp
 //                         redux over 64-bit (value, ~id) keys, then sigmoid
 //                         and renormalisation.
-//   chunk_hist_kernel     per 256-token chunk: one bit per (expert, token) in
-//                         shared memory -> per-chunk expert histogram.
+//   chunk_hist_kernel     per 256-token chunk (four threads per token): one bit
+//                         per (expert, token) in shared memory -> per-chunk
+//                         expert histogram.
 //   scan_kernel           one CTA: per-expert prefix over chunks, exclusive
 //                         scan over experts (offsets), 128-row tile schedule.
 //   maps_kernel           slot = expert offset + chunk prefix + popcount of the
@@ -29,6 +30,7 @@ namespace moe {
 namespace {
 
 constexpr int kChunk = 256;  // tokens per chunk of the histogram / maps kernels
+constexpr int kChunkThreads = 1024;  // 4 threads per token, each taking every 4th slot j
 
 __device__ __forceinline__ uint32_t order_key(float v) {
   const uint32_t u = __float_as_uint(v);
@@ -145,11 +147,12 @@ __device__ __forceinline__ void build_bits(uint32_t* bits, const int* __restrict
                                            int E, int k, int* err_flag, bool check) {
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bits[i] = 0u;
   __syncthreads();
-  const int t = blockIdx.x * kChunk + threadIdx.x;
+  const int tk = threadIdx.x % kChunk;  // token within the chunk
+  const int t = blockIdx.x * kChunk + tk;
   if (t < T) {
-    const uint32_t bit = 1u << (threadIdx.x & 31);
-    const int word = threadIdx.x >> 5;
-    for (int j = 0; j < k; ++j) {
+    const uint32_t bit = 1u << (tk & 31);
+    const int word = tk >> 5;
+    for (int j = threadIdx.x / kChunk; j < k; j += kChunkThreads / kChunk) {
       const int e = __ldg(idx + static_cast<size_t>(t) * k + j);
       if (e < 0 || e >= E) {
         if (check) set_flag(err_flag, MOE_FLAG_BAD_EXPERT);
@@ -162,9 +165,9 @@ __device__ __forceinline__ void build_bits(uint32_t* bits, const int* __restrict
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kChunk) chunk_hist_kernel(const int* __restrict__ idx, int T,
-                                                            int E, int k, int* __restrict__ hist,
-                                                            int* err_flag) {
+__global__ void __launch_bounds__(kChunkThreads)
+    chunk_hist_kernel(const int* __restrict__ idx, int T, int E, int k, int* __restrict__ hist,
+                      int* err_flag) {
   extern __shared__ uint32_t bits[];
   build_bits(bits, idx, T, E, k, err_flag, true);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -240,20 +243,18 @@ __global__ void __launch_bounds__(1024) scan_kernel(int* __restrict__ hist, int 
   for (long long r = rows_total + e; r < rows_cap; r += blockDim.x) token_of[r] = -1;
 }
 
-__global__ void __launch_bounds__(kChunk) maps_kernel(const int* __restrict__ idx, int T, int E,
-                                                      int k, const int* __restrict__ base,
-                                                      const int* __restrict__ offsets,
-                                                      const float* __restrict__ topk_w,
-                                                      int* __restrict__ slot_of,
-                                                      int* __restrict__ token_of,
-                                                      float* __restrict__ row_w) {
+__global__ void __launch_bounds__(kChunkThreads)
+    maps_kernel(const int* __restrict__ idx, int T, int E, int k, const int* __restrict__ base,
+                const int* __restrict__ offsets, const float* __restrict__ topk_w,
+                int* __restrict__ slot_of, int* __restrict__ token_of, float* __restrict__ row_w) {
   extern __shared__ uint32_t bits[];
   build_bits(bits, idx, T, E, k, nullptr, false);
-  const int t = blockIdx.x * kChunk + threadIdx.x;
+  const int tk = threadIdx.x % kChunk;
+  const int t = blockIdx.x * kChunk + tk;
   if (t >= T) return;
-  const int word = threadIdx.x >> 5;
-  const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
-  for (int j = 0; j < k; ++j) {
+  const int word = tk >> 5;
+  const uint32_t below = (1u << (tk & 31)) - 1u;
+  for (int j = threadIdx.x / kChunk; j < k; j += kChunkThreads / kChunk) {
     const size_t o = static_cast<size_t>(t) * k + j;
     const int e = __ldg(idx + o);
     if (e < 0 || e >= E) {
@@ -559,7 +560,7 @@ cudaError_t launch_permute_maps(const int* idx, const float* topk_w, int T, int 
   const size_t sm = static_cast<size_t>(E) * 8 * sizeof(uint32_t);
   {
     LaunchTimer lt("permute_hist", st);
-    chunk_hist_kernel<<<nch, kChunk, sm, st>>>(idx, T, E, k, hist_ws, err_flag);
+    chunk_hist_kernel<<<nch, kChunkThreads, sm, st>>>(idx, T, E, k, hist_ws, err_flag);
   }
   {
     LaunchTimer lt("permute_scan", st);
@@ -568,8 +569,8 @@ cudaError_t launch_permute_maps(const int* idx, const float* topk_w, int T, int 
   }
   {
     LaunchTimer lt("permute_maps", st);
-    maps_kernel<<<nch, kChunk, sm, st>>>(idx, T, E, k, hist_ws, offsets, topk_w, slot_of, token_of,
-                                         row_w);
+    maps_kernel<<<nch, kChunkThreads, sm, st>>>(idx, T, E, k, hist_ws, offsets, topk_w, slot_of,
+                                                token_of, row_w);
   }
   return cudaGetLastError();
 }
