@@ -254,6 +254,19 @@ def oracle_sample_time(inp_cpu, n_tokens):
     return time.perf_counter() - t0
 
 
+def host_threads() -> int:
+    """Threads the oracle's numpy BLAS calls may use: the BLAS/OpenMP thread limit
+    when one is set, else the cores this process may run on."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return int(v)
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     from sparse_moe_layer_topk_gb300 import inputs as I
@@ -270,7 +283,7 @@ def run_reference(args):
     times = [oracle_sample_time(inp, n) for _ in range(args.steps)]
     total = sum(times)
     value = n * args.steps / total
-    cores = os.cpu_count()
+    cores = host_threads()
     line.update({
         "value": value, "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * total / args.steps, "scaling": "weak", "vs_baseline": None,
@@ -548,7 +561,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         n = args.cpu_sample_tokens
         secs = oracle_sample_time(inp, n)
-        cpu = {"value": n / secs, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+        cpu = {"value": n / secs, "unit": "tokens/s", "cores": host_threads(), "kind": "oracle",
                "sample": f"fwd+bwd of the first {n} tokens of the workload, full weights, "
                          f"{secs:.1f} s"}
 
