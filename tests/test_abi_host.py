@@ -12,14 +12,33 @@ from sparse_moe_layer_topk_gb300 import build as B
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _declared():
+def _declarations():
+    """name -> (return type text, [argument texts]) of every moe_* prototype."""
     txt = open(os.path.join(ROOT, "include", "moe.h")).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    txt = re.sub(r"//[^\n]*", "", txt)
     decls = {}
-    for m in re.finditer(r"^\s*(?:const\s+)?[\w\s\*]+?\b(moe_\w+)\s*\(([^)]*)\)\s*;", txt, re.M):
-        args = [a for a in m.group(2).split(",") if a.strip() and a.strip() != "void"]
-        decls[m.group(1)] = len(args)
+    for m in re.finditer(r"^\s*((?:const\s+)?[\w\s\*]+?)\b(moe_\w+)\s*\(([^)]*)\)\s*;", txt, re.M):
+        args = [a.strip() for a in m.group(3).split(",") if a.strip() and a.strip() != "void"]
+        decls[m.group(2)] = (m.group(1).strip(), args)
     return decls
+
+
+def _declared():
+    return {name: len(args) for name, (_, args) in _declarations().items()}
+
+
+def _ctype_of(c_text):
+    """The ctypes type the binding must use for one C type (or argument) text."""
+    if "*" in c_text:
+        return M.ctypes.c_char_p if re.search(r"\bchar\s*\*", c_text) else M._P
+    if "size_t" in c_text:
+        return M._Z
+    if re.search(r"\bfloat\b", c_text):
+        return M._F
+    if re.search(r"\bint\b", c_text):
+        return M._I
+    raise AssertionError(f"unmapped C type: {c_text}")
 
 
 @pytest.fixture(scope="module")
@@ -35,6 +54,18 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
         assert hasattr(lib, name), name
         assert name in M.SIGNATURES, name
         assert len(M.SIGNATURES[name][0]) == nargs, (name, nargs)
+
+
+def test_binding_types_match_the_header():
+    """Every argument and return type of the ctypes binding is the one the header
+    declares (a pointer passed as an int, or a float as a pointer, would be
+    marshalled wrongly without any error)."""
+    for name, (ret, args) in _declarations().items():
+        argtypes, restype = M.SIGNATURES[name]
+        want = [_ctype_of(a) for a in args]
+        assert list(argtypes) == want, (name, [t.__name__ for t in argtypes],
+                                        [t.__name__ for t in want])
+        assert restype == _ctype_of(ret), (name, ret)
 
 
 def test_status_strings_and_version(lib):
