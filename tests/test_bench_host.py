@@ -1,0 +1,89 @@
+"""Host logic of bench.py (no GPU): the algorithmic work per launch that the
+roofline divides by, the choice and labelling of the peaks, and the whole-job
+throughput arithmetic."""
+import json
+
+import pytest
+
+import bench
+from sparse_moe_layer_topk_gb300 import inputs as I
+
+# the bench workload: T=16384 tokens, d=4096, l=1024, E=896 experts, top-16, f=512, 2 shared
+CFG = I.CONFIGS[4]
+T, d, l, E, k, f, S = CFG.T, CFG.d, CFG.l, CFG.E, CFG.k, CFG.f, CFG.S
+R = T * k
+
+
+def test_bench_workload_shape():
+    assert (T, d, l, E, k, f, S) == (16384, 4096, 1024, 896, 16, 512, 2)
+
+
+@pytest.mark.parametrize("label,flops,nbytes", [
+    # values worked out by hand from the shapes above (GFLOP, MB = 1e6 bytes)
+    ("router_logits_gemm", 120.26, None),      # 2 * 16384 * 4096 * 896
+    ("topk_sigmoid", 0, 61.87),                # 16384*896*4 + 16384*16*12
+    ("latent_proj_gemm", 137.44, None),        # 2 * 16384 * 4096 * 1024
+    ("permute_gather", 0, 571.47),             # 33.55 + 536.87 + 1.05
+    ("combine", 0, 605.03),                    # 536.87 + 2*33.55 + 1.05
+    ("expert_gemm1_swiglu", 549.76, None),     # 2 * 262144 * 1024 * 1024
+    ("expert_wgrad1", 549.76, 4831.84),        # 536.87 + 536.87 + 896*1024*1024*4
+    ("expert_wgrad2", 274.88, 2684.35),        # 268.44 + 536.87 + 896*512*1024*4
+    ("down_proj_router_dgrad", 257.70, None),  # 2 * 16384 * 4096 * (1024 + 896)
+])
+def test_kernel_work_matches_hand_computed_values(label, flops, nbytes):
+    fl, by = bench.kernel_work(CFG, T)[label]
+    assert fl / 1e9 == pytest.approx(flops, abs=0.01)
+    if nbytes is not None:
+        assert by / 1e6 == pytest.approx(nbytes, abs=0.01)
+
+
+def test_kernel_work_scales_with_tokens():
+    """Every routed and dense term is linear in T except the weights: doubling T
+    doubles the flops of every GEMM."""
+    a, b = bench.kernel_work(CFG, 4096), bench.kernel_work(CFG, 8192)
+    for label in a:
+        assert b[label][0] == 2 * a[label][0], label
+        assert b[label][1] >= a[label][1], label
+
+
+def test_peaks_exact_names():
+    p = {"hbm_gbs": 7100.0, "bf16_tflops": 2050.0, "bf16_tflops_sustained": 1750.0}
+    hbm, hs, tc, ts = bench.roofline_peaks(p)
+    assert (hbm, tc) == (7100.0, 1750.0)
+    assert hs.startswith("measured") and ts == "measured (sustained)"
+
+
+def test_peaks_nested_schema_and_value_objects():
+    p = {"hbm": {"copy": {"gbs": 6900.0, "bytes": 1 << 30}, "util_pct": 88.0},
+         "gemm": {"bf16": {"tflops": {"value": 2000.0}, "tflops_sustained": {"median": 1650.0}}},
+         "clocks": {"sm_mhz": 2070}}
+    hbm, hs, tc, ts = bench.roofline_peaks(p)
+    assert hbm == 6900.0 and hs == "measured (copy)"
+    assert tc == 1650.0 and ts == "measured (sustained)"
+
+
+def test_peaks_burst_only_is_labelled_as_burst():
+    hbm, hs, tc, ts = bench.roofline_peaks({"hbm_gbs": 7000, "bf16_tflops": 2000})
+    assert tc == 2000.0 and "burst" in ts
+
+
+def test_peaks_fallback_is_labelled_fallback():
+    for p in ({}, {"note": "no data"}, {"hbm_gbs": 0, "bf16_tflops": None}):
+        hbm, hs, tc, ts = bench.roofline_peaks(p)
+        assert hbm == bench.FALLBACK_PEAKS["hbm_gbs"] and hs == "fallback (copy)"
+        assert tc == bench.FALLBACK_PEAKS["bf16_tflops_sustained"] and ts == "fallback (sustained)"
+
+
+def test_peaks_file_reading(tmp_path):
+    path = tmp_path / "peaks.json"
+    assert bench.load_peaks(str(path)) == {}
+    path.write_text("not json")
+    assert bench.load_peaks(str(path)) == {}
+    path.write_text(json.dumps({"hbm_gbs": 7000}))
+    assert bench.load_peaks(str(path)) == {"hbm_gbs": 7000}
+
+
+def test_job_throughput_and_single_rank_time():
+    # 2 replicas x 16384 tokens x 10 steps in 50 ms of the slowest rank
+    assert bench.job_tokens_per_s(2, 16384, 10, 50.0) == pytest.approx(2 * 16384 * 10 / 0.05)
+    assert bench.max_over_ranks(12.5, 1, "cpu") == 12.5
