@@ -355,6 +355,47 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def roofline_report(per_kernel, work, peaks, traffic_of):
+    """(roofline of the dominant kernel, per-kernel breakdown, grouped-GEMM % of bf16 peak).
+
+    per_kernel: label -> (launches, total ms) over the timed steps; work: label ->
+    algorithmic (flops, bytes) per launch; peaks: the tuple of roofline_peaks;
+    traffic_of(label): ncu DRAM bytes per launch on record for that kernel, or None.
+    A kernel's floor is the larger of its compute time and its memory time at the
+    peaks; the dominant kernel (largest total time) is reported against whichever
+    of the two bounds it."""
+    hbm, hbm_src, tc, tc_src = peaks
+    total = sum(v[1] for v in per_kernel.values())
+    breakdown = {}
+    for name, (cnt, tot) in sorted(per_kernel.items(), key=lambda kv: -kv[1][1]):
+        fl, by = work.get(name, (0, 0))
+        avg_s = tot / cnt / 1000.0
+        floor_s = max(fl / (tc * 1e12), by / (hbm * 1e9))
+        breakdown[name] = {"launches": cnt, "avg_us": round(avg_s * 1e6, 2),
+                           "share": round(tot / total, 4),
+                           "tflops": round(fl / avg_s / 1e12, 1) if fl else None,
+                           "gbs": round(by / avg_s / 1e9, 1),
+                           "roofline_frac": round(floor_s / avg_s, 3) if floor_s else None}
+    roof = None
+    if per_kernel:
+        name, (cnt, tot) = max(per_kernel.items(), key=lambda kv: kv[1][1])
+        fl, by = work.get(name, (0, 0))
+        avg_s = tot / cnt / 1000.0
+        if fl and fl / (tc * 1e12) >= by / (hbm * 1e9):
+            roof = {"kernel": name, "bound": "tensor", "achieved": fl / avg_s / 1e12,
+                    "peak": tc, "unit": "TFLOP/s", "frac": fl / avg_s / 1e12 / tc}
+        else:
+            roof = {"kernel": name, "bound": "hbm", "achieved": by / avg_s / 1e9, "peak": hbm,
+                    "unit": "GB/s", "frac": by / avg_s / 1e9 / hbm}
+        roof["traffic"] = traffic_of(name)
+        roof["avg_launch_us"] = avg_s * 1e6
+        roof["peak_source"] = tc_src if roof["bound"] == "tensor" else hbm_src
+    g_fl = sum(work[n][0] * per_kernel[n][0] for n in EXPERT_GEMMS if n in per_kernel)
+    g_ms = sum(per_kernel[n][1] for n in EXPERT_GEMMS if n in per_kernel)
+    grouped_pct = 100.0 * (g_fl / (g_ms / 1000.0) / 1e12) / tc if g_ms else None
+    return roof, breakdown, grouped_pct
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def _event_time(fn, steps, warmup, stream):
@@ -572,37 +613,10 @@ def run_ours(args):
         raise RuntimeError(f"device error flag {int(layer.err.item())}")
 
     # ---- roofline of the dominant kernel
-    hbm, hbm_src, tc, tc_src = roofline_peaks(load_peaks())
-    work = kernel_work(cfg, T)
-    top = max(per_kernel.items(), key=lambda kv: kv[1][1]) if per_kernel else None
-    roof = None
-    breakdown = {}
-    for name, (cnt, tot) in sorted(per_kernel.items(), key=lambda kv: -kv[1][1]):
-        fl, by = work.get(name, (0, 0))
-        avg_s = tot / cnt / 1000.0
-        floor_s = max(fl / (tc * 1e12), by / (hbm * 1e9))
-        breakdown[name] = {"launches": cnt, "avg_us": round(avg_s * 1e6, 2),
-                           "share": round(tot / sum(v[1] for v in per_kernel.values()), 4),
-                           "tflops": round(fl / avg_s / 1e12, 1) if fl else None,
-                           "gbs": round(by / avg_s / 1e9, 1),
-                           "roofline_frac": round(floor_s / avg_s, 3) if floor_s else None}
-    if top:
-        name, (cnt, tot) = top
-        fl, by = work.get(name, (0, 0))
-        avg_s = tot / cnt / 1000.0
-        # the bound is whichever of compute time and memory time is larger
-        if fl and fl / (tc * 1e12) >= by / (hbm * 1e9):
-            roof = {"kernel": name, "bound": "tensor", "achieved": fl / avg_s / 1e12,
-                    "peak": tc, "unit": "TFLOP/s", "frac": fl / avg_s / 1e12 / tc}
-        else:
-            roof = {"kernel": name, "bound": "hbm", "achieved": by / avg_s / 1e9, "peak": hbm,
-                    "unit": "GB/s", "frac": by / avg_s / 1e9 / hbm}
-        roof["traffic"] = dram_traffic(name, cfg.name)
-        roof["avg_launch_us"] = avg_s * 1e6
-        roof["peak_source"] = tc_src if roof["bound"] == "tensor" else hbm_src
-    g_fl = sum(work[n][0] * per_kernel[n][0] for n in EXPERT_GEMMS if n in per_kernel)
-    g_ms = sum(per_kernel[n][1] for n in EXPERT_GEMMS if n in per_kernel)
-    grouped_pct = 100.0 * (g_fl / (g_ms / 1000.0) / 1e12) / tc if g_ms else None
+    peaks = roofline_peaks(load_peaks())
+    tc, tc_src = peaks[2], peaks[3]
+    roof, breakdown, grouped_pct = roofline_report(per_kernel, kernel_work(cfg, T), peaks,
+                                                   lambda name: dram_traffic(name, cfg.name))
 
     secondary = None
     if rank == 0 and not args.no_secondary and not (args.tokens or args.experts):

@@ -87,3 +87,35 @@ def test_job_throughput_and_single_rank_time():
     # 2 replicas x 16384 tokens x 10 steps in 50 ms of the slowest rank
     assert bench.job_tokens_per_s(2, 16384, 10, 50.0) == pytest.approx(2 * 16384 * 10 / 0.05)
     assert bench.max_over_ranks(12.5, 1, "cpu") == 12.5
+
+
+def test_roofline_report_picks_the_dominant_kernel_and_its_bound():
+    peaks = (8000.0, "measured (copy)", 2000.0, "measured (sustained)")
+    work = {"mem_kernel": (1e9, 8e9),      # 0.5 ms of compute, 1.0 ms of memory at the peaks
+            "tc_kernel": (4e12, 1e9),      # 2.0 ms of compute, 0.125 ms of memory
+            "tiny": (0, 1e6)}
+    # label -> (launches, total ms)
+    per = {"mem_kernel": (2, 4.0), "tc_kernel": (1, 2.5), "tiny": (4, 0.4)}
+    roof, br, gp = bench.roofline_report(per, work, peaks, lambda name: 123)
+    assert roof["kernel"] == "mem_kernel" and roof["bound"] == "hbm"
+    assert roof["achieved"] == pytest.approx(8e9 / 2e-3 / 1e9)       # 4000 GB/s per launch
+    assert roof["frac"] == pytest.approx(0.5) and roof["traffic"] == 123
+    assert roof["peak"] == 8000.0 and roof["peak_source"] == "measured (copy)"
+    assert br["tc_kernel"]["roofline_frac"] == pytest.approx(2.0 / 2.5)
+    assert br["tc_kernel"]["tflops"] == pytest.approx(1600.0)
+    assert sum(v["share"] for v in br.values()) == pytest.approx(1.0, abs=1e-3)
+    assert list(br) == ["mem_kernel", "tc_kernel", "tiny"]   # by total time
+    assert gp is None                                          # no expert GEMM timed
+
+    per = {"tc_kernel": (1, 2.5), "tiny": (1, 0.1)}
+    roof, _, _ = bench.roofline_report(per, work, peaks, lambda name: None)
+    assert roof["bound"] == "tensor" and roof["unit"] == "TFLOP/s"
+    assert roof["frac"] == pytest.approx(0.8) and roof["peak_source"] == "measured (sustained)"
+
+
+def test_roofline_report_grouped_gemm_percentage():
+    peaks = (8000.0, "m", 2000.0, "m")
+    work = {n: (1e12, 1e9) for n in bench.EXPERT_GEMMS}
+    per = {n: (2, 2.0) for n in bench.EXPERT_GEMMS}             # 1 ms per launch
+    _, _, gp = bench.roofline_report(per, work, peaks, lambda name: None)
+    assert gp == pytest.approx(100.0 * 1000.0 / 2000.0)       # 1 PFLOP/s of 2
