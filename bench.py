@@ -117,7 +117,10 @@ def kernel_work(cfg, T):
         "latent_proj_dgrad": (2 * T * d * l, T * d * b + d * l * b + T * l * b),
         "latent_proj_wgrad": (2 * T * d * l, T * d * b + T * l * b + d * l * 4),
         "combine_bwd_gather": (0, T * l * b + R * l * b + R * 4),
-        "expert_dgrad2_swiglu_bwd": (2 * R * l * f, R * l * b + w2 + R * 6 * f * b + R * f * b + R * 8),
+        # dy and W2 in; the epilogue reads g, u, h and writes dg, du, w*h (6 f per
+        # row) and the routing-weight gradient (its per-n-tile partials are the
+        # engine's, not the algorithm's)
+        "expert_dgrad2_swiglu_bwd": (2 * R * l * f, R * l * b + w2 + R * 6 * f * b + R * 4),
         "expert_wgrad2": (2 * R * f * l, R * f * b + R * l * b + E * f * l * 4),
         "expert_dgrad1": (2 * R * 2 * f * l, R * 2 * f * b + w13 + R * l * b),
         "expert_wgrad1": (2 * R * l * 2 * f, R * l * b + R * 2 * f * b + E * l * 2 * f * 4),
@@ -126,7 +129,8 @@ def kernel_work(cfg, T):
         "shared_dgrad1": (2 * T * S * 2 * f * l, T * S * 2 * f * b + S * l * 2 * f * b + T * l * b),
         "shared_wgrad1": (2 * T * l * S * 2 * f, T * l * b + T * S * 2 * f * b + S * l * 2 * f * 4),
         "permute_bwd_sum": (0, R * l * b + 2 * T * l * b + R * 4),
-        "routing_weight_grad_reduce": (0, R * 8 + R * 4),
+        # two epilogue warps per lane quadrant x one partial per 256-wide n tile
+        "routing_weight_grad_reduce": (0, R * 4 * 2 * ((f + 255) // 256) + R * 4),
         "router_bwd_dlogits": (0, T * k * 16 + T * E * b),
         "router_dgrad": (2 * T * E * d, T * E * b + d * E * b + 2 * T * d * b),
         "down_proj_router_dgrad": (2 * T * d * (l + E),

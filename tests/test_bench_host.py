@@ -29,6 +29,9 @@ def test_bench_workload_shape():
     ("expert_wgrad1", 549.76, 4831.84),        # 536.87 + 536.87 + 896*1024*1024*4
     ("expert_wgrad2", 274.88, 2684.35),        # 268.44 + 536.87 + 896*512*1024*4
     ("down_proj_router_dgrad", 257.70, None),  # 2 * 16384 * 4096 * (1024 + 896)
+    # dy 536.87 + W2 939.52 + g,u,h in and dg,du,w*h out 1610.61 + d_row_w 1.05
+    ("expert_dgrad2_swiglu_bwd", 274.88, 3088.06),
+    ("routing_weight_grad_reduce", 0, 5.24),   # 4 fp32 partials in, 1 out, per row
 ])
 def test_kernel_work_matches_hand_computed_values(label, flops, nbytes):
     fl, by = bench.kernel_work(CFG, T)[label]
