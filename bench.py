@@ -97,13 +97,15 @@ def dist_env():
 
 # ---------------------------------------------------------------- algorithmic work
 
-def kernel_work(cfg, T):
-    """Algorithmic (flops, bytes) per launch of each kernel label at token count T."""
+def kernel_work(cfg, T, wgrad_bytes=4):
+    """Algorithmic (flops, bytes) per launch of each kernel label at token count T;
+    weight gradients are written as fp32 (wgrad_bytes=4) or bf16 (2)."""
     d, l, E, k, S, f = cfg.d, cfg.l, cfg.E, cfg.k, cfg.S, cfg.f
     R = T * k
     w13 = E * l * 2 * f * 2
     w2 = E * f * l * 2
     b = 2  # bf16 bytes
+    g = wgrad_bytes
     return {
         "router_logits_gemm": (2 * T * d * E, T * d * b + d * E * b + T * E * 4),
         "topk_sigmoid": (0, T * E * 4 + T * k * 12),
@@ -115,19 +117,19 @@ def kernel_work(cfg, T):
         "shared_gemm2": (2 * T * S * f * l, T * S * f * b + S * f * l * b + T * l * b),
         "combine": (0, R * l * b + 2 * T * l * b + R * 4),
         "latent_proj_dgrad": (2 * T * d * l, T * d * b + d * l * b + T * l * b),
-        "latent_proj_wgrad": (2 * T * d * l, T * d * b + T * l * b + d * l * 4),
+        "latent_proj_wgrad": (2 * T * d * l, T * d * b + T * l * b + d * l * g),
         "combine_bwd_gather": (0, T * l * b + R * l * b + R * 4),
         # dy and W2 in; the epilogue reads g, u, h and writes dg, du, w*h (6 f per
         # row) and the routing-weight gradient (its per-n-tile partials are the
         # engine's, not the algorithm's)
         "expert_dgrad2_swiglu_bwd": (2 * R * l * f, R * l * b + w2 + R * 6 * f * b + R * 4),
-        "expert_wgrad2": (2 * R * f * l, R * f * b + R * l * b + E * f * l * 4),
+        "expert_wgrad2": (2 * R * f * l, R * f * b + R * l * b + E * f * l * g),
         "expert_dgrad1": (2 * R * 2 * f * l, R * 2 * f * b + w13 + R * l * b),
-        "expert_wgrad1": (2 * R * l * 2 * f, R * l * b + R * 2 * f * b + E * l * 2 * f * 4),
+        "expert_wgrad1": (2 * R * l * 2 * f, R * l * b + R * 2 * f * b + E * l * 2 * f * g),
         "shared_dgrad2_swiglu_bwd": (2 * T * l * S * f, T * l * b + S * f * l * b + T * S * 5 * f * b),
-        "shared_wgrad2": (2 * T * S * f * l, T * S * f * b + T * l * b + S * f * l * 4),
+        "shared_wgrad2": (2 * T * S * f * l, T * S * f * b + T * l * b + S * f * l * g),
         "shared_dgrad1": (2 * T * S * 2 * f * l, T * S * 2 * f * b + S * l * 2 * f * b + T * l * b),
-        "shared_wgrad1": (2 * T * l * S * 2 * f, T * l * b + T * S * 2 * f * b + S * l * 2 * f * 4),
+        "shared_wgrad1": (2 * T * l * S * 2 * f, T * l * b + T * S * 2 * f * b + S * l * 2 * f * g),
         "permute_bwd_sum": (0, R * l * b + 2 * T * l * b + R * 4),
         # two epilogue warps per lane quadrant x one partial per 256-wide n tile
         "routing_weight_grad_reduce": (0, R * 4 * 2 * ((f + 255) // 256) + R * 4),
@@ -135,7 +137,7 @@ def kernel_work(cfg, T):
         "router_dgrad": (2 * T * E * d, T * E * b + d * E * b + 2 * T * d * b),
         "down_proj_router_dgrad": (2 * T * d * (l + E),
                                    T * (l + E) * b + d * (l + E) * b + T * d * b),
-        "router_wgrad": (2 * T * d * E, T * d * b + T * E * b + d * E * 4),
+        "router_wgrad": (2 * T * d * E, T * d * b + T * E * b + d * E * g),
     }
 
 
@@ -619,7 +621,8 @@ def run_ours(args):
     # ---- roofline of the dominant kernel
     peaks = roofline_peaks(load_peaks())
     tc, tc_src = peaks[2], peaks[3]
-    roof, breakdown, grouped_pct = roofline_report(per_kernel, kernel_work(cfg, T), peaks,
+    work = kernel_work(cfg, T, 4 if args.wgrad == "f32" else 2)
+    roof, breakdown, grouped_pct = roofline_report(per_kernel, work, peaks,
                                                    lambda name: dram_traffic(name, cfg.name))
 
     secondary = None

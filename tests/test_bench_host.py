@@ -122,3 +122,13 @@ def test_roofline_report_grouped_gemm_percentage():
     per = {n: (2, 2.0) for n in bench.EXPERT_GEMMS}             # 1 ms per launch
     _, _, gp = bench.roofline_report(per, work, peaks, lambda name: None)
     assert gp == pytest.approx(100.0 * 1000.0 / 2000.0)       # 1 PFLOP/s of 2
+
+
+def test_kernel_work_bf16_weight_gradients():
+    """With bf16 weight gradients only the gradient writes shrink, by half."""
+    a, b = bench.kernel_work(CFG, T), bench.kernel_work(CFG, T, wgrad_bytes=2)
+    grads = {"latent_proj_wgrad": d * l, "expert_wgrad2": E * f * l, "expert_wgrad1": E * l * 2 * f,
+             "shared_wgrad2": S * f * l, "shared_wgrad1": S * l * 2 * f, "router_wgrad": d * E}
+    for label in a:
+        assert a[label][0] == b[label][0], label
+        assert a[label][1] - b[label][1] == 2 * grads.get(label, 0), label
