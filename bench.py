@@ -622,8 +622,10 @@ def run_ours(args):
     peaks = roofline_peaks(load_peaks())
     tc, tc_src = peaks[2], peaks[3]
     work = kernel_work(cfg, T, 4 if args.wgrad == "f32" else 2)
-    roof, breakdown, grouped_pct = roofline_report(per_kernel, work, peaks,
-                                                   lambda name: dram_traffic(name, cfg.name))
+    # the DRAM traffic on record was captured with fp32 weight gradients
+    roof, breakdown, grouped_pct = roofline_report(
+        per_kernel, work, peaks,
+        lambda name: dram_traffic(name, cfg.name) if args.wgrad == "f32" else None)
 
     secondary = None
     if rank == 0 and not args.no_secondary and not (args.tokens or args.experts):
