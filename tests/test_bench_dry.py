@@ -153,3 +153,16 @@ def test_bf16_gradients_and_eager_timing():
     assert d["roofline"]["traffic"] is None        # the capture on record used fp32 gradients
     assert d["timing"]["value"] == "eager launches"
     assert d["config"]["wgrad_dtype"] == "bf16"
+
+
+def test_reference_arm_runs_on_rank_0_only(monkeypatch, capsys):
+    """Under torchrun the oracle arm runs and prints on rank 0 alone; the other
+    ranks return at once without work or output."""
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    with mock.patch.object(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2"]):
+        args = bench.parse()
+    with mock.patch.object(bench, "oracle_sample_time", side_effect=AssertionError("work on rank 1")):
+        assert bench.run_reference(args) is None
+    assert capsys.readouterr().out == ""
