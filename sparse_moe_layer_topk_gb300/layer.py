@@ -218,27 +218,31 @@ class LatentMoELayer:
                 loaded[i] = ev()
                 loaded[i].record(h2d)
 
+        keep = self.dx  # the eager steps write their input gradient into the slots
         load(0)
-        for i in range(n):
-            s = i & 1
-            if i + 1 < n:
-                load(i + 1)
-            comp.wait_event(loaded[i])
-            if i >= 2:
-                comp.wait_event(drained[i - 2])  # dx slot s copied out by step i-2
-            if graphs:
-                self._pipe_graphs[s].replay()
-            else:
-                self.forward(P["x"][s])
-                self.dx = P["dx"][s]  # the backward writes the input gradient into slot s
-                self.backward(P["g"][s])
-            computed[i] = ev()
-            computed[i].record(comp)
-            with torch.cuda.stream(d2h):
-                d2h.wait_event(computed[i])
-                dx_host[i].copy_(P["dx"][s], non_blocking=True)
-                drained[i] = ev()
-                drained[i].record(d2h)
+        try:
+            for i in range(n):
+                s = i & 1
+                if i + 1 < n:
+                    load(i + 1)
+                comp.wait_event(loaded[i])
+                if i >= 2:
+                    comp.wait_event(drained[i - 2])  # dx slot s copied out by step i-2
+                if graphs:
+                    self._pipe_graphs[s].replay()
+                else:
+                    self.forward(P["x"][s])
+                    self.dx = P["dx"][s]
+                    self.backward(P["g"][s])
+                computed[i] = ev()
+                computed[i].record(comp)
+                with torch.cuda.stream(d2h):
+                    d2h.wait_event(computed[i])
+                    dx_host[i].copy_(P["dx"][s], non_blocking=True)
+                    drained[i] = ev()
+                    drained[i].record(d2h)
+        finally:
+            self.dx = keep
         comp.wait_event(drained[n - 1])
 
 
