@@ -68,6 +68,44 @@ def test_binding_types_match_the_header():
         assert restype == _ctype_of(ret), (name, ret)
 
 
+def test_wrapper_parameters_follow_the_header_order():
+    """Each Python wrapper names its parameters as the header does, in the same
+    order, so two arguments of one C type cannot be swapped unnoticed (`in` is a
+    Python keyword and becomes `inp`)."""
+    import inspect
+    # entry points the binding calls directly, or wraps with another interface
+    unwrapped = {"moe_status_string", "moe_last_cuda_error", "moe_timing_report"}
+    for name, (_, args) in _declarations().items():
+        if name in unwrapped:
+            continue
+        header = [re.findall(r"(\w+)\s*$", a.replace("*", " "))[0] for a in args]
+        header = ["inp" if h == "in" else h for h in header]
+        params = list(inspect.signature(getattr(M, name)).parameters)
+        assert params == header, (name, params, header)
+        # and hands them to the library in that order
+        passed = _call_args(getattr(M, name))
+        if passed is not None:
+            assert passed == [name] + params, (name, passed)
+
+
+def _call_args(fn):
+    """The arguments of the wrapper's `_call(...)` as names (the entry point's
+    name as its string), or None when the wrapper does not use _call."""
+    import ast
+    import inspect
+    import textwrap
+    tree = ast.parse(textwrap.dedent(inspect.getsource(fn)))
+    for node in ast.walk(tree):
+        if isinstance(node, ast.Call) and getattr(node.func, "id", None) == "_call":
+            out = []
+            for a in node.args:
+                if isinstance(a, ast.Call) and getattr(a.func, "id", None) in ("int", "float"):
+                    a = a.args[0]  # a plain conversion of the argument
+                out.append(a.value if isinstance(a, ast.Constant) else getattr(a, "id", None))
+            return out
+    return None
+
+
 def test_status_strings_and_version(lib):
     assert lib.moe_version() >= 1
     for code in (M.MOE_OK, M.MOE_ERR_ARG, M.MOE_ERR_ALIGN, M.MOE_ERR_WORKSPACE,
