@@ -98,13 +98,27 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     return _lib
 
 
+_EMPTY = {}
+
+
+def _empty_ptr(device):
+    """A valid, aligned device address standing for an array of zero elements:
+    the library refuses null pointers and never touches a zero-length array."""
+    t = _EMPTY.get(device)
+    if t is None:
+        t = _EMPTY[device] = torch.empty(256, dtype=torch.uint8, device=device)
+    return t.data_ptr()
+
+
 def _ptr(x):
     if x is None:
         return None
     if isinstance(x, torch.Tensor):
-        if x.numel() and not x.is_cuda:
-            raise MoEError("libmoe takes device tensors")
-        return x.data_ptr() if x.numel() else None
+        if not x.is_cuda:
+            if x.numel():
+                raise MoEError("libmoe takes device tensors")
+            return None
+        return x.data_ptr() if x.numel() else _empty_ptr(x.device)
     return int(x)
 
 

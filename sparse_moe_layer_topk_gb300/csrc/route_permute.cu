@@ -558,16 +558,17 @@ cudaError_t launch_permute_maps(const int* idx, const float* topk_w, int T, int 
                                 cudaStream_t st) {
   const int nch = permute_chunks(T);
   const size_t sm = static_cast<size_t>(E) * 8 * sizeof(uint32_t);
-  {
+  if (nch > 0) {
     LaunchTimer lt("permute_hist", st);
     chunk_hist_kernel<<<nch, kChunkThreads, sm, st>>>(idx, T, E, k, hist_ws, err_flag);
   }
   {
+    // with no tokens the scan alone writes the zero counts, offsets and schedule
     LaunchTimer lt("permute_scan", st);
     scan_kernel<<<1, 1024, 0, st>>>(hist_ws, nch, E, static_cast<long long>(T) * k, counts,
                                     offsets, tile_sched, token_of);
   }
-  {
+  if (nch > 0) {
     LaunchTimer lt("permute_maps", st);
     maps_kernel<<<nch, kChunkThreads, sm, st>>>(idx, T, E, k, hist_ws, offsets, topk_w, slot_of,
                                                 token_of, row_w);

@@ -156,3 +156,19 @@ def test_argument_errors_before_any_cuda_call(lib):
     # an auxiliary-loss gradient needs the batch's mean routing distribution
     assert lib.moe_route_topk_bwd(P, P, P, P, P, P, P, 64, 64, 64, 4, None, None, None, 0, P, None,
                                   None, 1.0, None, None, 0, P, 1 << 30, None, None) == M.MOE_ERR_ARG
+
+
+def test_zero_tokens_enqueue_nothing(lib):
+    """With T = 0 the forward calls and the row-movement backward calls return
+    MOE_OK before any CUDA call (this host has no GPU, so any call would fail)."""
+    P = 0x1000
+    assert lib.moe_router_logits(P, P, 0, 64, 64, P, None) == M.MOE_OK
+    assert lib.moe_topk_from_logits(P, None, 0, 64, 4, P, P, P, None, None) == M.MOE_OK
+    assert lib.moe_route_topk(P, P, None, 0, 64, 64, 4, P, P, P, P, 256, None, None) == M.MOE_OK
+    assert lib.moe_latent_proj(P, P, 0, 64, 64, P, None) == M.MOE_OK
+    assert lib.moe_latent_proj_bwd(P, P, P, 0, 64, 64, P, None, 0, None) == M.MOE_OK
+    assert lib.moe_grouped_swiglu(P, P, P, P, P, P, 4, 0, 64, 64, P, P, P, None) == M.MOE_OK
+    assert lib.moe_shared_swiglu(P, P, P, 0, 64, 64, 1, P, P, P, None) == M.MOE_OK
+    assert lib.moe_unpermute_combine(P, P, None, 0, 4, 64, P, None) == M.MOE_OK
+    assert lib.moe_unpermute_combine_bwd(P, P, 0, 4, 64, P, None) == M.MOE_OK
+    assert lib.moe_permute_bwd(P, P, None, 0, 4, 64, P, None) == M.MOE_OK
