@@ -132,3 +132,19 @@ def test_kernel_work_bf16_weight_gradients():
     for label in a:
         assert a[label][0] == b[label][0], label
         assert a[label][1] - b[label][1] == 2 * grads.get(label, 0), label
+
+
+def test_clock_samples_parsing():
+    out = "\n".join([
+        "2070, 2070, 910.55, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "2055, 2070, 1398.20, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "[N/A], 2070, [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]",   # a sample the driver could not read
+        "2040, 2070, 1401.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "garbage",
+    ])
+    c = bench.parse_clock_samples(out)
+    assert c == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    hot = bench.parse_clock_samples(
+        "1800, 2070, 1400, 0x28, Not Active, Active, Active, Not Active\n")
+    assert hot["reasons"] == ["hw_thermal_slowdown", "sw_thermal_slowdown"]
+    assert bench.parse_clock_samples("")["sm_mhz"] is None
