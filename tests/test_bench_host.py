@@ -148,3 +148,17 @@ def test_clock_samples_parsing():
         "1800, 2070, 1400, 0x28, Not Active, Active, Active, Not Active\n")
     assert hot["reasons"] == ["hw_thermal_slowdown", "sw_thermal_slowdown"]
     assert bench.parse_clock_samples("")["sm_mhz"] is None
+
+
+def test_dram_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
+    """The recorded ncu traffic is reported only while the GEMM engine's sources
+    hash to the value it was captured on, and only for its own workload."""
+    tab = json.load(open(bench.os.path.join(bench.ROOT, "profiles", "dram_traffic.json")))
+    wl = "latentmoe_fwd_bwd_T16384_E896_top16"
+    ent = tab[wl]["expert_wgrad1"]
+    monkeypatch.setattr(bench, "source_hash", lambda: ent["source_hash"])
+    assert bench.dram_traffic("expert_wgrad1", wl) == ent["bytes_per_launch"]
+    assert bench.dram_traffic("expert_wgrad1", "another_workload") is None
+    assert bench.dram_traffic("no_such_kernel", wl) is None
+    monkeypatch.setattr(bench, "source_hash", lambda: "0" * 16)
+    assert bench.dram_traffic("expert_wgrad1", wl) is None
