@@ -171,7 +171,8 @@ int moe_permute_noalloc(const uint16_t* z, const int32_t* topk_idx, const float*
  * Output: pieces[i][4] = {expert, rank, first row within the expert's
  * segment, rows} for i < *n_pieces (capacity 2E + P pieces, int32),
  * rank_load[P] = rows per rank (max = C). Runs on the device from the counts
- * of moe_permute (no host synchronisation). E + P <= 2048. */
+ * of moe_permute (no host synchronisation). E + P <= 2048. Counts that are
+ * negative or sum to 2^31 or more give *n_pieces = -1 and no plan. */
 int moe_replica_plan(const int32_t* counts, int E, int P, int32_t* pieces, int32_t* n_pieces,
                      int32_t* rank_load, void* stream);
 

@@ -683,7 +683,17 @@ __global__ void replica_plan_kernel(const int* __restrict__ counts, int E, int P
   if (threadIdx.x != 0) return;
   const int per = E / P;
   long long R = 0;
-  for (int e = 0; e < E; ++e) R += counts[e];
+  for (int e = 0; e < E; ++e) {
+    if (counts[e] < 0) {  // not a count: no plan
+      *n_pieces = -1;
+      return;
+    }
+    R += counts[e];
+  }
+  if (R >= (1ll << 31)) {
+    *n_pieces = -1;
+    return;
+  }
   const int C = static_cast<int>((R + P - 1) / P);
   int n = 0;
   for (int r = 0; r < P; ++r) {
@@ -702,7 +712,12 @@ __global__ void replica_plan_kernel(const int* __restrict__ counts, int E, int P
   for (int e = 0; e < E; ++e) {
     int r = 0;
     while (done[e] < counts[e]) {
-      while (load[r] >= C) ++r;
+      // P * C >= R rows, so a rank with spare capacity remains while rows do
+      while (r < P && load[r] >= C) ++r;
+      if (r == P) {
+        *n_pieces = -1;
+        return;
+      }
       const int take = min(counts[e] - done[e], C - load[r]);
       pieces[4 * n] = e; pieces[4 * n + 1] = r; pieces[4 * n + 2] = done[e]; pieces[4 * n + 3] = take;
       ++n;
