@@ -41,6 +41,11 @@
  *    reads it when it chooses. Rows with a bad expert id are skipped.
  *  - Dimension limits: l, f, d multiples of 64; E <= 1024 (and a multiple of
  *    64 where a GEMM has E columns); 1 <= k <= min(E, 32); T*k < 2^31.
+ *  - Index arrays that moe_permute writes (offsets, tile_sched, slot_of,
+ *    token_of) are trusted by the calls that read them: pass them as written,
+ *    or with the same invariants. A negative slot or token entry means "no
+ *    row"; other entries are not range-checked on the device. Expert ids
+ *    (topk_idx) are checked, as above.
  *  - Weight layouts: W13 [E][l][2f] (gate columns 0..f-1, up columns f..2f-1),
  *    W2 [E][f][l]; shared experts use the same layout with E -> S; Wr [d][E],
  *    W_dn [d][l], W_up [l][d].
