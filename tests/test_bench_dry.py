@@ -111,6 +111,7 @@ def run(argv):
         mock.patch.object(LY, "weights_to_device", lambda inp: {}),
         mock.patch.object(bench, "ClockSampler", FakeClocks),
         mock.patch.object(bench, "oracle_sample_time", lambda inp, n: 11.5),
+        mock.patch.object(bench, "load_peaks", lambda *a, **k: {}),  # no measured peaks
     ]
     for p in patches:
         p.start()
@@ -144,6 +145,7 @@ def test_json_line_has_every_contract_key():
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["clocks"]["sm_mhz"] > 0
+    assert d["secondary_peak"] == {"tflops": 1900.0, "source": "fallback (burst)"}
     json.dumps(d)
 
 

@@ -162,3 +162,10 @@ def test_dram_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
     assert bench.dram_traffic("no_such_kernel", wl) is None
     monkeypatch.setattr(bench, "source_hash", lambda: "0" * 16)
     assert bench.dram_traffic("expert_wgrad1", wl) is None
+
+
+def test_burst_peak_for_kernels_timed_alone():
+    assert bench.burst_tc_peak({"bf16_tflops": 2050.0, "bf16_tflops_sustained": 1700.0}) == \
+        (2050.0, "measured (burst)")
+    assert bench.burst_tc_peak({"bf16_tflops_sustained": 1700.0}) == \
+        (bench.FALLBACK_PEAKS["bf16_tflops"], "fallback (burst)")
