@@ -451,3 +451,16 @@ def test_bucket_order_invariants(seed):
     tiles = [(int(counts[e]) + 127) // 128 for e in order]
     assert sched.tolist() == [0] + np.cumsum(tiles).tolist()
     assert sched[-1] == O.m_tiles_schedule(counts)[-1]
+
+
+def test_empty_batch_closed_form():
+    """No tokens: empty outputs and input gradient, zero counts and offsets, and
+    every weight gradient exactly zero (each is a sum over no tokens)."""
+    inp = I.make_layer_inputs(0, T=0)
+    cfg = inp["cfg"]
+    fwd = O.layer_forward(inp)
+    bwd = O.layer_backward(inp, fwd)
+    assert fwd["out"].shape == (0, cfg.d) and bwd["dx"].shape == (0, cfg.d)
+    assert not np.any(fwd["counts"]) and not np.any(fwd["offsets"])
+    for name in ("dWr", "dW_dn", "dW13", "dW2", "dW13_sh", "dW2_sh", "dW_up"):
+        assert bwd[name].shape and not np.any(bwd[name]), name
