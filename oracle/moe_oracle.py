@@ -198,18 +198,24 @@ def combine(y_perm, slot_of, y_shared=None):
 # Whole layer
 # --------------------------------------------------------------------------
 
-def layer_forward(inp: dict, k: int | None = None, T: slice | None = None) -> dict:
+def layer_forward(inp: dict, k: int | None = None, idx=None) -> dict:
     """Forward of the latent MoE layer on the bf16 inputs of `inp`.
 
     out = (y_sh + sum_j w_j o_j) W_up with z = x W_dn, o_j = expert_j(z),
     y_sh = sum_s SwiGLU_s(z) (shared experts in latent space, weight 1),
-    routing on x as above. Returns every intermediate (fp64)."""
+    routing on x as above. Returns every intermediate (fp64).
+
+    Staged parity: `idx` [T,k], when given, replaces the selection step (a
+    selection decided on logits of another precision, where a token whose
+    k-th and (k+1)-th logits are closer than that precision's rounding may
+    pick another last expert); the weights still follow from the fp64 logits
+    of the selected experts, and every later step is unchanged."""
     cfg = inp["cfg"]
     k = cfg.k if k is None else k
     x = _f64(inp["x"])
     E = cfg.E
     L = router_logits(x, inp["Wr"], inp.get("bias"))
-    idx = topk_select(L, k)
+    idx = topk_select(L, k) if idx is None else np.asarray(idx, dtype=np.int64)
     w, s = routing_weights(L, idx)
     z = x @ _f64(inp["W_dn"])
     slot_of, token_of, offsets = permutation_maps(idx, E)

@@ -80,6 +80,19 @@ def test_topk_equal_columns_lower_id_wins():
         assert pos[7] == pos[3] + 1 and pos[9] == pos[3] + 2
 
 
+def test_topk_signed_zeros_are_one_value():
+    """-0.0 == +0.0, so zeros of either sign tie and the lower id goes first."""
+    L = np.array([[0.0, -0.0, 1.0, -0.0, 0.0, -2.0],
+                  [-0.0, 0.0, -1.0, 0.0, -0.0, 3.0]])
+    assert O.topk_select(L, 4).tolist() == [[2, 0, 1, 3], [5, 0, 1, 3]]
+    rng = np.random.default_rng(8)
+    M = rng.choice(np.array([-0.0, 0.0, 1.0, -1.0]), size=(50, 12))
+    for k in (1, 3, 12):
+        idx = O.topk_select(M, k)
+        for t in range(50):
+            assert idx[t].tolist() == _brute_topk(M[t].tolist(), k)
+
+
 def test_topk_k_equals_E_is_full_order():
     L = I.make_logits(3, 8, 12).numpy().astype(np.float64)
     idx = O.topk_select(L, 12)
