@@ -32,8 +32,11 @@ namespace {
 constexpr int kChunk = 256;  // tokens per chunk of the histogram / maps kernels
 constexpr int kChunkThreads = 1024;  // 4 threads per token, each taking every 4th slot j
 
+// Order-preserving bits of a float; -0 and +0 are one value (they compare
+// equal, so a tie between them goes to the lower expert id like any other).
 __device__ __forceinline__ uint32_t order_key(float v) {
-  const uint32_t u = __float_as_uint(v);
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

@@ -88,6 +88,39 @@ def test_topk_from_logits_bit_exact(T, E, k, ties, bias):
     assert int(err.item()) == 0
 
 
+@pytest.mark.parametrize("neg_zero_bias", [False, True])
+def test_topk_signed_zero_ties(neg_zero_bias):
+    """-0.0 and +0.0 are equal logits: when they tie at the k-th place the
+    lower expert id wins, whatever the signs. With a bias of -0.0 the summed
+    value keeps the sign of the logit (-0 + -0 = -0), so signed zeros reach
+    the selection itself."""
+    T, E, k = 97, 64, 4
+    rng = np.random.default_rng(5)
+    L = -rng.uniform(1.0, 5.0, size=(T, E)).astype(np.float32)
+    for t in range(T):
+        top = rng.choice(E, size=k - 1, replace=False)
+        L[t, top] = rng.uniform(1.0, 2.0, size=k - 1)
+        rest = np.setdiff1d(np.arange(E), top)
+        zeros = rng.choice(rest, size=6, replace=False)
+        L[t, zeros] = np.where(rng.random(6) < 0.5, np.float32(-0.0), np.float32(0.0))
+    # the lowest-id zero of some tokens is a -0.0 that an order with -0 < +0 would skip
+    assert any(np.signbit(L[t, np.where(L[t] == 0)[0].min()]) for t in range(T))
+    b = torch.full((E,), -0.0, dtype=torch.float32) if neg_zero_bias else None
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    s = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.moe_topk_from_logits(dev(torch.from_numpy(L)), dev(b) if b is not None else None, T, E, k,
+                           idx, w, s, err)
+    torch.cuda.synchronize()
+    ref_idx = O.topk_select(L.astype(np.float64), k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    ref_w, ref_s = O.routing_weights(L.astype(np.float64), ref_idx)
+    np.testing.assert_allclose(s.cpu().numpy(), ref_s, rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=3e-6, atol=1e-7)
+    assert int(err.item()) == 0
+
+
 def test_topk_flags_nonfinite():
     L = I.make_logits(1, 16, 64)
     L[3, 5] = float("nan")
