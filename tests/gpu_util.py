@@ -41,6 +41,31 @@ def check_close(name, got, ref, max_abs=MAX_ABS, rel_fro=REL_FRO, scale_by_max=F
     return mx, fro
 
 
+def check_close_chunked(name, got, ref, chunk=32, max_abs=MAX_ABS, rel_fro=REL_FRO,
+                        scale_by_max=False):
+    """check_close of a large tensor `got` (torch, any device) against `ref`
+    (numpy fp64): the same two criteria, accumulated over slices of axis 0 so
+    that no full-size fp64 temporary is made."""
+    ref = np.asarray(ref)
+    assert tuple(got.shape) == ref.shape, (name, tuple(got.shape), ref.shape)
+    mx = se = sr = mref = 0.0
+    for i in range(0, ref.shape[0], chunk):
+        g = f64(got[i:i + chunk])
+        r = np.asarray(ref[i:i + chunk], dtype=np.float64)
+        assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+        d = np.abs(g - r)
+        if d.size:
+            mx = max(mx, float(d.max()))
+            mref = max(mref, float(np.abs(r).max()))
+        se += float(np.sum(d * d))
+        sr += float(np.sum(r * r))
+    if scale_by_max and mref > 0:
+        mx /= mref
+    fro = np.sqrt(se / sr) if sr > 0 else np.sqrt(se)
+    assert mx <= max_abs and fro <= rel_fro, f"{name}: max_err={mx:.3e} rel_fro={fro:.3e}"
+    return mx, fro
+
+
 def dev(t, dtype=None):
     t = t if dtype is None else t.to(dtype)
     return t.contiguous().cuda()

@@ -17,7 +17,7 @@ from sparse_moe_layer_topk_gb300 import _lib as M
 from sparse_moe_layer_topk_gb300 import inputs as I
 from sparse_moe_layer_topk_gb300.layer import LatentMoELayer, weights_to_device
 
-from gpu_util import check_close, f64, need_gpu
+from gpu_util import check_close, check_close_chunked, f64, need_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -115,34 +115,96 @@ def test_layer_single_token():
     assert not layer.grads["W13"][empty].any() and not layer.grads["W2"][empty].any()
 
 
+def _gpu_logits(layer):
+    """The fp32 router logits the GPU selected on (they stay in the route
+    workspace after the forward)."""
+    T, E = layer.T, layer.E
+    return layer.ws["route"][: T * E * 4].view(torch.float32).view(T, E).cpu().numpy()
+
+
+def _check_routing_staged(layer, k, L_ref, max_bad, bias=None):
+    """Staged routing parity at full size: the oracle's selection step run on the
+    values the GPU decides on (its own fp32 logits, plus the bias in fp32 when
+    there is one) must give the GPU's ids bit for bit, and its weights (sigmoid
+    and renormalisation of those fp32 values) to fp32 rounding; those values
+    must be within fp32 accumulation error of the fp64 logits L_ref (bias
+    included); and against L_ref only rare near-ties may select another expert.
+    Returns the GPU's ids and the tokens whose selection differs from the fp64
+    one."""
+    v32 = _gpu_logits(layer)
+    if bias is not None:
+        v32 = (v32 + bias.numpy()[None, :]).astype(np.float32)
+    v32 = v32.astype(np.float64)
+    assert np.abs(v32 - L_ref).max() < 1e-3
+    gi = layer.topk_idx.cpu().numpy()
+    np.testing.assert_array_equal(gi, O.topk_select(v32, k))
+    w32, s32 = O.routing_weights(v32, gi)
+    np.testing.assert_allclose(layer.topk_s.cpu().numpy(), s32, rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(layer.topk_w.cpu().numpy(), w32, rtol=3e-6, atol=1e-7)
+    bad, _ = _routing_disagreement(layer, L_ref, k)
+    assert bad.size <= max_bad, bad.size
+    return gi, bad
+
+
+def _check_maps(layer, gi, E):
+    """Counts, offsets, slot and token maps, tile schedule and permuted routing
+    weights of the GPU's permute against the oracle's counting sort of the GPU's
+    ids: bit for bit."""
+    slot_of, token_of, offsets = O.permutation_maps(gi, E)
+    counts = np.diff(offsets)
+    np.testing.assert_array_equal(layer.counts.cpu().numpy(), counts)
+    np.testing.assert_array_equal(layer.offsets.cpu().numpy(), offsets)
+    np.testing.assert_array_equal(layer.slot_of.cpu().numpy(), slot_of)
+    np.testing.assert_array_equal(layer.token_of.cpu().numpy(), token_of)
+    np.testing.assert_array_equal(layer.tile_sched.cpu().numpy(), O.m_tiles_schedule(counts, 128))
+    row_w = np.empty(gi.size, dtype=np.float32)
+    row_w[slot_of.reshape(-1)] = layer.topk_w.cpu().numpy().reshape(-1)
+    np.testing.assert_array_equal(layer.row_w.cpu().numpy(), row_w)
+    return counts
+
+
 @pytest.mark.parametrize("cfg_id", [1, 2])
 def test_layer_full_size_forward(cfg_id):
     inp = I.make_layer_inputs(cfg_id)
     cfg = inp["cfg"]
     layer = _run(inp, backward=False)
     fwd = O.layer_forward(inp)
-    bad, _ = _routing_disagreement(layer, fwd["L"], cfg.k)
-    assert bad.size <= max(2, cfg.T // 1000), bad.size
+    gi, bad = _check_routing_staged(layer, cfg.k, fwd["L"], max(2, cfg.T // 1000), inp["bias"])
+    counts = _check_maps(layer, gi, cfg.E)
     keep = np.setdiff1d(np.arange(cfg.T), bad)
     check_close("out", f64(layer.out)[keep], fwd["out"][keep])
     check_close("y_lat", f64(layer.y_lat)[keep], fwd["y_lat"][keep])
-    if bad.size == 0:
-        # same expert sets: counts, offsets and each token's expert -> slot map
-        # are unique; the order of a token's experts may differ where two of its
-        # selected logits are closer than the fp32 rounding
-        np.testing.assert_array_equal(layer.counts.cpu().numpy(), fwd["counts"])
-        np.testing.assert_array_equal(layer.offsets.cpu().numpy(), fwd["offsets"])
-        gi, gs = layer.topk_idx.cpu().numpy(), layer.slot_of.cpu().numpy()
-        og, os_ = np.argsort(gi, 1), np.argsort(fwd["idx"], 1)
-        np.testing.assert_array_equal(np.take_along_axis(gs, og, 1),
-                                      np.take_along_axis(fwd["slot_of"], os_, 1))
-        reordered = np.where((gi != fwd["idx"]).any(1))[0]
-        for t in reordered:
-            Lsel = fwd["L"][t, fwd["idx"][t]]
-            assert np.min(np.abs(np.diff(np.sort(Lsel)))) < 1e-3
     if cfg.skew:
-        counts = layer.counts.cpu().numpy()
         assert (counts <= 2).sum() >= 150 and (counts == 0).sum() > 0
+
+
+def test_layer_T2048_E896_every_output_and_gradient():
+    """The layer at the 896-expert shapes (d=4096, l=1024, E=896 top-16, S=2,
+    f=512) with T=2048 tokens: every output and every gradient (out, dx, d_w,
+    dWr, dW_dn, dW13, dW2, dW13_sh, dW2_sh, dW_up) against the full fp64 oracle
+    on the same inputs. This runs the router's 896 columns (three 256-wide
+    tiles and a 128-wide tail) in the logits and in dWr, and the K-split
+    shared-expert weight gradients (2 slices at K = 2048). Routing is staged:
+    the GPU's ids are checked bit for bit against the oracle's selection on the
+    GPU's fp32 logits, and the oracle then runs on those ids, so no token is
+    excluded from any comparison."""
+    inp = I.make_layer_inputs(1, T=2048)
+    cfg = inp["cfg"]
+    layer = _run(inp)
+    L = O.router_logits(inp["x"], inp["Wr"], inp["bias"])
+    gi, _ = _check_routing_staged(layer, cfg.k, L, 4)
+    _check_maps(layer, gi, cfg.E)
+    fwd = O.layer_forward(inp, idx=gi)
+    check_close("w", f64(layer.topk_w), fwd["w"], max_abs=1e-5, rel_fro=1e-5)
+    for name in ("z", "y_lat", "out"):
+        check_close(name, f64(getattr(layer, name)), fwd[name])
+    check_close_chunked("z_perm", layer.z_perm, fwd["z_perm"], chunk=4096)
+    check_close_chunked("y_perm", layer.y_perm, fwd["y_perm"], chunk=4096)
+    bwd = O.layer_backward(inp, fwd)
+    check_close("dx", f64(layer.dx), bwd["dx"])
+    check_close("d_w", f64(layer.d_topk_w), bwd["d_w"])
+    for wn, gn in GRAD_NAMES.items():
+        check_close_chunked(gn, layer.grads[wn], bwd[gn], scale_by_max=True)
 
 
 def test_ep_rank_grouped_gemm_and_return():
@@ -171,27 +233,38 @@ def test_ep_rank_grouped_gemm_and_return():
 
 
 def test_layer_fwd_bwd_T16384_sampled():
-    """The benchmark workload at full size (T=16384): every output and input
-    gradient of sampled tokens, and the expert weight gradients of sampled
-    experts, against the oracle run on exactly the tokens they depend on; the
-    dense weight gradients against their defining products of the layer's
-    own activations."""
+    """The benchmark workload at full size (T=16384).
+    - Routing and maps: staged, bit for bit, over all tokens.
+    - Every output and input gradient of sampled tokens (out, z, y_lat, dy_lat,
+      dz, d_w, dx) against the oracle run on exactly those tokens.
+    - Expert weight gradients of sampled experts against the oracle run on the
+      tokens they hold.
+    - The shared experts' weight gradients (and z, dy_lat, dz_sh over all
+      tokens) against the full fp64 oracle: they do not depend on the routing.
+    - dWr (896 columns: three 256-wide tiles and a 128-wide tail) against the
+      oracle's router backward fed the GPU's routing-weight gradients (checked
+      on the sampled tokens above) and x^T dL in fp64.
+    - dW_up and dW_dn against their defining products of the layer's own
+      y_lat and dz (both checked per token above)."""
     inp = I.make_layer_inputs(4)
     cfg = inp["cfg"]
     layer = _run(inp)
     L = O.router_logits(inp["x"], inp["Wr"], inp["bias"])
-    bad, ref_idx = _routing_disagreement(layer, L, cfg.k)
-    assert bad.size <= 20, bad.size
+    gpu_idx, bad = _check_routing_staged(layer, cfg.k, L, 20)
+    _check_maps(layer, gpu_idx, cfg.E)
+    ref_idx = O.topk_select(L, cfg.k)
     rng = np.random.default_rng(0)
     toks = np.setdiff1d(rng.choice(cfg.T, 96, replace=False), bad)
     sub = dict(inp)
     sub["x"], sub["g"] = inp["x"][toks], inp["g"][toks]
     fwd = O.layer_forward(sub)
     bwd = O.layer_backward(sub, fwd)
-    check_close("out", f64(layer.out)[toks], fwd["out"])
-    check_close("dx", f64(layer.dx)[toks], bwd["dx"])
+    for name in ("out", "z", "y_lat"):
+        check_close(name, f64(getattr(layer, name))[toks], fwd[name])
+    for name in ("dy_lat", "dz", "dx"):
+        check_close(name, f64(getattr(layer, name))[toks], bwd[name])
+    check_close("d_w", f64(layer.d_topk_w)[toks], bwd["d_w"])
     # sampled experts whose token set is the same on both sides
-    gpu_idx = layer.topk_idx.cpu().numpy()
     touched = set(np.unique(gpu_idx[bad])) | set(np.unique(ref_idx[bad]))
     cand = [e for e in rng.permutation(cfg.E) if e not in touched][:6]
     for e in cand:
@@ -202,11 +275,28 @@ def test_layer_fwd_bwd_T16384_sampled():
         be = O.layer_backward(sub, fe)
         check_close(f"dW13[{e}]", f64(layer.grads["W13"][e]), be["dW13"][e], scale_by_max=True)
         check_close(f"dW2[{e}]", f64(layer.grads["W2"][e]), be["dW2"][e], scale_by_max=True)
+    # shared experts over all tokens: full oracle
+    x, g = f64(inp["x"]), f64(inp["g"])
+    z_ref = x @ f64(inp["W_dn"])
+    dy_ref = g @ f64(inp["W_up"]).T
+    check_close("z (all tokens)", f64(layer.z), z_ref)
+    check_close("dy_lat (all tokens)", f64(layer.dy_lat), dy_ref)
+    dz_sh = np.zeros_like(z_ref)
+    for s in range(cfg.S):
+        dzs, dW13s, dW2s = O.swiglu_expert_backward(z_ref, inp["W13_sh"][s], inp["W2_sh"][s],
+                                                    dy_ref)
+        dz_sh += dzs
+        check_close(f"dW13_sh[{s}]", f64(layer.grads["W13_sh"][s]), dW13s, scale_by_max=True)
+        check_close(f"dW2_sh[{s}]", f64(layer.grads["W2_sh"][s]), dW2s, scale_by_max=True)
+    check_close("dz_sh (all tokens)", f64(layer.dz_sh), dz_sh)
+    del dz_sh, z_ref, dy_ref
+    # router weight gradient: the oracle's router backward on the GPU's d_w
+    dL = O.router_backward(f64(layer.d_topk_w), f64(layer.topk_w), f64(layer.topk_s), gpu_idx,
+                           cfg.E)
+    check_close("dWr", f64(layer.grads["Wr"]), x.T @ dL, scale_by_max=True)
     # dense weight gradients = their defining products on the layer's activations
-    check_close("dW_up", f64(layer.grads["W_up"]), f64(layer.y_lat).T @ f64(inp["g"]),
-                scale_by_max=True)
-    check_close("dW_dn", f64(layer.grads["W_dn"]), f64(inp["x"]).T @ f64(layer.dz),
-                scale_by_max=True)
+    check_close("dW_up", f64(layer.grads["W_up"]), f64(layer.y_lat).T @ g, scale_by_max=True)
+    check_close("dW_dn", f64(layer.grads["W_dn"]), x.T @ f64(layer.dz), scale_by_max=True)
 
 
 def test_layer_cfg0_with_aux_balance_loss():
