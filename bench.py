@@ -55,6 +55,11 @@ def parse():
                     help="profiling case: override T (the JSON line then names that case)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling case: override E (the JSON line then names that case)")
+    ap.add_argument("--case", default="", choices=["", "topk", "permute", "gather", "combine"],
+                    help="time one entry point alone on the workload's sizes (for ncu): "
+                         "topk = moe_topk_from_logits on fp32 logits [T][E]; permute = "
+                         "moe_permute; gather = moe_unpermute_combine_bwd; combine = "
+                         "moe_unpermute_combine")
     return ap.parse_args()
 
 
@@ -134,11 +139,23 @@ def kernel_work(cfg, T, wgrad_bytes=4):
         # two epilogue warps per lane quadrant x one partial per 256-wide n tile
         "routing_weight_grad_reduce": (0, R * 4 * 2 * ((f + 255) // 256) + R * 4),
         "router_bwd_dlogits": (0, T * k * 16 + T * E * b),
-        "router_dgrad": (2 * T * E * d, T * E * b + d * E * b + 2 * T * d * b),
-        "down_proj_router_dgrad": (2 * T * d * (l + E),
-                                   T * (l + E) * b + d * (l + E) * b + T * d * b),
-        "router_wgrad": (2 * T * d * E, T * d * b + T * E * b + d * E * g),
+        # The router backward's logit gradient dL has k nonzeros per token: its
+        # algorithmic cost is 2 T k d per product, reading the k (value, id)
+        # pairs per token (6 bytes each); the dense GEMMs that run it execute
+        # the flops of DENSE_EXECUTED (the difference is counted as waste)
+        "router_dgrad": (2 * T * k * d, T * k * 6 + d * E * b + 2 * T * d * b),
+        "down_proj_router_dgrad": (2 * T * d * l + 2 * T * k * d,
+                                   T * l * b + d * l * b + T * k * 6 + d * E * b + T * d * b),
+        "router_wgrad": (2 * T * k * d, T * d * b + T * k * 6 + d * E * g),
     }
+
+
+def dense_executed_flops(cfg, T):
+    """Flops the dense router-backward GEMMs execute per launch (their
+    algorithmic cost, in kernel_work, is the sparse 2 T k d per product)."""
+    d, l, E = cfg.d, cfg.l, cfg.E
+    return {"router_dgrad": 2 * T * E * d, "down_proj_router_dgrad": 2 * T * d * (l + E),
+            "router_wgrad": 2 * T * d * E}
 
 
 def load_peaks(path=None):
@@ -377,7 +394,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def roofline_report(per_kernel, work, peaks, traffic_of):
+def roofline_report(per_kernel, work, peaks, traffic_of, executed=None):
     """(roofline of the dominant kernel, per-kernel breakdown, grouped-GEMM % of bf16 peak).
 
     per_kernel: label -> (launches, total ms) over the timed steps; work: label ->
@@ -385,7 +402,9 @@ def roofline_report(per_kernel, work, peaks, traffic_of):
     traffic_of(label): ncu DRAM bytes per launch on record for that kernel, or None.
     A kernel's floor is the larger of its compute time and its memory time at the
     peaks; the dominant kernel (largest total time) is reported against whichever
-    of the two bounds it."""
+    of the two bounds it. executed: label -> flops a launch executes where that
+    exceeds its algorithmic flops (dense GEMMs over sparse operands); such kernels
+    also report the executed rate and the executed flops' share that is waste."""
     hbm, hbm_src, tc, tc_src = peaks
     total = sum(v[1] for v in per_kernel.values())
     breakdown = {}
@@ -398,6 +417,10 @@ def roofline_report(per_kernel, work, peaks, traffic_of):
                            "tflops": round(fl / avg_s / 1e12, 1) if fl else None,
                            "gbs": round(by / avg_s / 1e9, 1),
                            "roofline_frac": round(floor_s / avg_s, 3) if floor_s else None}
+        if executed and name in executed:
+            ex = executed[name]
+            breakdown[name]["executed_tflops"] = round(ex / avg_s / 1e12, 1)
+            breakdown[name]["executed_waste_frac"] = round(1.0 - fl / ex, 4) if ex else None
     roof = None
     if per_kernel:
         name, (cnt, tot) = max(per_kernel.items(), key=lambda kv: kv[1][1])
@@ -644,7 +667,8 @@ def run_ours(args):
     # the DRAM traffic on record was captured with fp32 weight gradients
     roof, breakdown, grouped_pct = roofline_report(
         per_kernel, work, peaks,
-        lambda name: dram_traffic(name, cfg.name) if args.wgrad == "f32" else None)
+        lambda name: dram_traffic(name, cfg.name) if args.wgrad == "f32" else None,
+        executed=dense_executed_flops(cfg, T))
 
     secondary = None
     if rank == 0 and not args.no_secondary and not (args.tokens or args.experts):
@@ -690,10 +714,70 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- single entry points
+
+def entry_point_case(name, T, E, k, l):
+    """A closure that calls one libmoe entry point on synthetic inputs of the
+    given sizes; only the buffers that entry point touches are allocated."""
+    import torch
+
+    from sparse_moe_layer_topk_gb300 import _lib as M
+    from sparse_moe_layer_topk_gb300 import inputs as I
+    dev = "cuda"
+    if name == "topk":
+        L = I.make_logits(1, T, E).to(dev)
+        idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+        w = torch.empty(T, k, dtype=torch.float32, device=dev)
+        s = torch.empty(T, k, dtype=torch.float32, device=dev)
+        return lambda: M.moe_topk_from_logits(L, None, T, E, k, idx, w, s)
+    ids = I.make_topk_ids(2, T, E, k).to(dev)
+    R = T * k
+    if name == "permute":
+        z = torch.randn(T, l, device=dev).to(torch.bfloat16)
+        zp = torch.empty(R, l, dtype=torch.bfloat16, device=dev)
+        bufs = [torch.empty(n, dtype=torch.int32, device=dev) for n in (E, E + 1, R, R, E + 1)]
+        wsb = M.moe_workspace_size(M.MOE_OP_PERMUTE, T=T, E=E)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        return lambda: M.moe_permute(z, ids, None, T, l, E, k, zp, bufs[0], bufs[1], bufs[2],
+                                     bufs[3], bufs[4], None, ws, wsb)
+    perm = torch.randperm(R, generator=torch.Generator().manual_seed(3))
+    token_of = (perm // k).to(torch.int32).to(dev)
+    slot_of = torch.empty(R, dtype=torch.int32)
+    slot_of[perm] = torch.arange(R, dtype=torch.int32)
+    slot_of = slot_of.to(dev)
+    if name == "gather":
+        src = torch.randn(T, l, device=dev).to(torch.bfloat16)
+        dst = torch.empty(R, l, dtype=torch.bfloat16, device=dev)
+        return lambda: M.moe_unpermute_combine_bwd(src, token_of, T, k, l, dst)
+    yp = torch.randn(R, l, device=dev).to(torch.bfloat16)
+    ysh = torch.randn(T, l, device=dev).to(torch.bfloat16)
+    out = torch.empty(T, l, dtype=torch.bfloat16, device=dev)
+    return lambda: M.moe_unpermute_combine(yp, slot_of, ysh, T, k, l, out)
+
+
+def run_case(args):
+    """One entry point alone, `--steps` calls after `--warmup`, CUDA-event timed
+    (a case for ncu captures of single kernels); prints one JSON line."""
+    import torch
+
+    from sparse_moe_layer_topk_gb300 import _lib as M
+    from sparse_moe_layer_topk_gb300 import build as B
+    B.build_library()
+    M.load()
+    cfg = workload(args)
+    fn = entry_point_case(args.case, cfg.T, cfg.E, cfg.k, cfg.l)
+    ms = _event_time(fn, args.steps, max(1, args.warmup), torch.cuda.current_stream())
+    print(json.dumps({"case": args.case, "workload": cfg.name, "T": cfg.T, "E": cfg.E,
+                      "k": cfg.k, "l": cfg.l, "avg_us": 1000.0 * ms, "calls": args.steps}),
+          flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.case:
+        run_case(args)
     else:
         run_ours(args)
 

@@ -28,7 +28,9 @@ def test_bench_workload_shape():
     ("expert_gemm1_swiglu", 549.76, None),     # 2 * 262144 * 1024 * 1024
     ("expert_wgrad1", 549.76, 4831.84),        # 536.87 + 536.87 + 896*1024*1024*4
     ("expert_wgrad2", 274.88, 2684.35),        # 268.44 + 536.87 + 896*512*1024*4
-    ("down_proj_router_dgrad", 257.70, None),  # 2 * 16384 * 4096 * (1024 + 896)
+    # the router backward's dL has 16 nonzeros per token: 2 T k d per product
+    ("down_proj_router_dgrad", 139.59, None),  # 2*16384*4096*1024 + 2*16384*16*4096
+    ("router_wgrad", 2.15, 150.47),            # x 134.22 + 16 (value, id) pairs/token 1.57 + dWr 14.68
     # dy 536.87 + W2 939.52 + g,u,h in and dg,du,w*h out 1610.61 + d_row_w 1.05
     ("expert_dgrad2_swiglu_bwd", 274.88, 3088.06),
     ("routing_weight_grad_reduce", 0, 5.24),   # 4 fp32 partials in, 1 out, per row
@@ -169,3 +171,23 @@ def test_burst_peak_for_kernels_timed_alone():
         (2050.0, "measured (burst)")
     assert bench.burst_tc_peak({"bf16_tflops_sustained": 1700.0}) == \
         (bench.FALLBACK_PEAKS["bf16_tflops"], "fallback (burst)")
+
+
+def test_dense_router_backward_executed_flops_and_waste():
+    """The dense GEMMs of the router backward execute 2 T E d flops per product;
+    the breakdown reports that rate and the share of it that is waste next to
+    the roofline fraction, which is taken on the sparse algorithmic cost."""
+    ex = bench.dense_executed_flops(CFG, T)
+    assert ex["router_wgrad"] / 1e9 == pytest.approx(120.26, abs=0.01)
+    assert ex["down_proj_router_dgrad"] / 1e9 == pytest.approx(257.70, abs=0.01)
+    work = bench.kernel_work(CFG, T)
+    peaks = (6800.0, "m", 1700.0, "m")
+    per = {"router_wgrad": (1, 0.082), "down_proj_router_dgrad": (1, 0.139)}
+    _, br, _ = bench.roofline_report(per, work, peaks, lambda name: None, executed=ex)
+    assert br["router_wgrad"]["executed_tflops"] == pytest.approx(120.26e9 / 82e-6 / 1e12, rel=1e-3)
+    assert br["router_wgrad"]["executed_waste_frac"] == pytest.approx(1 - 16 / 896, abs=1e-4)
+    # memory floor of router_wgrad: reading x once (plus dL's nonzeros and dWr)
+    assert br["router_wgrad"]["roofline_frac"] == pytest.approx(150.47e6 / 6800e9 / 82e-6, rel=1e-2)
+    # compute floor of the fused dgrad: its down-projection part plus the sparse router part
+    assert br["down_proj_router_dgrad"]["roofline_frac"] == pytest.approx(
+        139.59e9 / 1700e12 / 139e-6, rel=1e-2)
