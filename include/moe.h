@@ -354,6 +354,18 @@ int moe_route_topk_bwd(const float* d_row_w, const int32_t* slot_of, const int32
 int moe_timing_enable(int on);
 int moe_timing_report(char* buf, size_t len);
 
+/* Check of the bounded waits. Every wait of a library kernel on an mbarrier
+ * (a copy landing, an accumulator filling or draining) gives up after a time
+ * limit, ORs MOE_FLAG_TIMEOUT into the caller's error word and lets the kernel
+ * return, so a wait that can never end does not hang the GPU. This call runs
+ * that same wait, with the limit `limit_ns` (1e3 .. 1e9 ns), in one thread of
+ * a one-warp kernel, on an mbarrier that nothing arrives at: it always times
+ * out, sets MOE_FLAG_TIMEOUT in *err_flag (device int32) and writes the
+ * nanoseconds it waited to *waited_ns (device int64). It uses no TMA copy, no
+ * tensor map and no tensor memory. The pages describe nothing like it. */
+int moe_diag_wait_timeout(long long limit_ns, int32_t* err_flag, long long* waited_ns,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,7 @@ SIGNATURES = {
     "moe_expert_buckets": ([_P, _I, _P, _P, _P], _I),
     "moe_grouped_swiglu_ordered": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P],
                                    _I),
+    "moe_diag_wait_timeout": ([ctypes.c_longlong, _P, _P, _P], _I),
     "moe_timing_enable": ([_I], _I),
     "moe_timing_report": ([ctypes.c_char_p, _Z], _I),
 }
@@ -254,6 +255,10 @@ def moe_route_topk_bwd(d_row_w, slot_of, topk_idx, topk_w, topk_s, x, Wr, T, d, 
 
 def moe_router_aux_loss(logits, bias, T, E, p_mean, loss, ws, ws_bytes, stream=None):
     _call("moe_router_aux_loss", logits, bias, T, E, p_mean, loss, ws, ws_bytes, stream)
+
+
+def moe_diag_wait_timeout(limit_ns, err_flag, waited_ns, stream=None):
+    _call("moe_diag_wait_timeout", int(limit_ns), err_flag, waited_ns, stream)
 
 
 def moe_timing_enable(on: bool):

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ["gemm_tc.cu", "route_permute.cu", "abi.cu", "timing.cu", "permute_noalloc.cu"]
+SOURCES = ["gemm_tc.cu", "route_permute.cu", "abi.cu", "timing.cu", "permute_noalloc.cu", "diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

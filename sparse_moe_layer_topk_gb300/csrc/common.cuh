@@ -81,10 +81,12 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t addr, uint32_t p
 }
 
 // Waits for the phase of `bar` with the given parity to complete. Returns false
-// (without completing) when `abort` becomes non-zero or the timeout expires.
-// CLUSTER: acquire at cluster scope (arrivals from the other CTA of a pair).
+// (without completing) when `abort` becomes non-zero or `limit_ns` of wall time
+// have passed. CLUSTER: acquire at cluster scope (arrivals from the other CTA
+// of a pair).
 template <bool CLUSTER = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns = kWaitTimeoutNs) {
   const uint32_t a = smem_u32(bar);
   auto try_once = [&]() {
     return CLUSTER ? mbar_test_wait_cluster(a, parity) : mbar_try_wait(a, parity);
@@ -96,7 +98,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 32; ++i)
       if (try_once()) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -34,6 +34,8 @@ def _ctype_of(c_text):
         return M.ctypes.c_char_p if re.search(r"\bchar\s*\*", c_text) else M._P
     if "size_t" in c_text:
         return M._Z
+    if re.search(r"\blong\s+long\b", c_text):
+        return M.ctypes.c_longlong
     if re.search(r"\bfloat\b", c_text):
         return M._F
     if re.search(r"\bint\b", c_text):

@@ -156,3 +156,32 @@ def test_shared_swiglu_writes_stay_in_bounds(T, l, f, S):
     M.moe_shared_swiglu_bwd(dy, z, W13, W2, gu, h, T, l, f, S, dz, dW13, dW2, M.MOE_DTYPE_F32, ws,
                             wsb)
     g.check()
+
+
+def test_bounded_wait_gives_up_sets_the_flag_and_leaves_the_gpu_usable():
+    """The library's mbarrier wait, with a 1 ms limit, on a barrier that nothing
+    arrives at: the kernel returns, MOE_FLAG_TIMEOUT is set, the wait lasted at
+    least the limit (and not unboundedly longer), and a layer step right after
+    still matches the fp64 oracle with a clean error word."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    M.moe_diag_wait_timeout(1_000_000, err, waited)
+    torch.cuda.synchronize()
+    assert int(err.item()) == M.MOE_FLAG_TIMEOUT
+    assert 1_000_000 <= int(waited.item()) < 200_000_000
+    with pytest.raises(M.MoEError):
+        M.moe_diag_wait_timeout(10, err, waited)   # limit out of range: nothing launched
+
+    from sparse_moe_layer_topk_gb300.layer import LatentMoELayer, weights_to_device
+    from gpu_util import check_close, f64
+    inp = I.make_layer_inputs(0)
+    cfg = inp["cfg"]
+    layer = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32)
+    out = layer.forward(inp["x"].cuda())
+    dx = layer.backward(inp["g"].cuda())
+    torch.cuda.synchronize()
+    assert int(layer.err.item()) == 0
+    fwd = O.layer_forward(inp)
+    bwd = O.layer_backward(inp, fwd)
+    check_close("out", f64(out), fwd["out"])
+    check_close("dx", f64(dx), bwd["dx"])
