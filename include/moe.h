@@ -157,9 +157,13 @@ int moe_permute(const uint16_t* z, const int32_t* topk_idx, const float* topk_w,
  * (held on every GPU that loads the library until it is unloaded), so it
  * handles permute_chunks(T) * E <= 262144, i.e. ceil(T / 256) * E <= 262144
  * (T <= 74,752 at E = 896); larger problems return MOE_ERR_WORKSPACE without
- * launching anything. The first call on a device looks up the array's device
- * address; make that first call before any stream capture. All calls share the
- * array: calls that may overlap on the GPU must be serialised by the caller. */
+ * launching anything. The first call on a device (and the first one after the
+ * device's current CUDA context changed, e.g. after cudaDeviceReset) looks up
+ * the array's device address; make that first call before any stream capture.
+ * All calls share the array, which keeps the last call's contents (no entry of
+ * it needs to start at zero): calls that may overlap on the GPU race on it and
+ * must be serialised by the caller. MOE_ERR_CUDA, when the address lookup
+ * fails, comes with its cause in moe_last_cuda_error(). */
 int moe_permute_noalloc(const uint16_t* z, const int32_t* topk_idx, const float* topk_w, int T,
                         int l, int E, int k, uint16_t* z_perm, int32_t* counts, int32_t* offsets,
                         int32_t* slot_of, int32_t* token_of, int32_t* tile_sched, float* row_w,

@@ -10,12 +10,15 @@
 // scratch in a fixed array in the library's own device memory instead.
 //
 // The array below lives in every GPU that loads the library, for as long as
-// the library stays loaded. Its device address is looked up once per device,
-// on the first call made on that device; make that first call before any
-// stream capture. All calls share the one array: calls that overlap on the
-// GPU (on different streams, or from several threads) race on it and must be
-// serialised by the caller. No entry of it has to start at zero: every entry
-// a call reads was written earlier in the same call.
+// the library stays loaded. Its device address is looked up on the first call
+// made on a device (and again if that device's current context has changed
+// since, e.g. after a cudaDeviceReset); make that first call before any stream
+// capture. All calls share the one array: calls that overlap on the GPU (on
+// different streams, or from several threads) race on it and must be
+// serialised by the caller. No entry of it has to start at zero: every entry a
+// call reads was written earlier in the same call.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -32,23 +35,60 @@ static __device__ __align__(256) int g_permute_scratch[kNoAllocScratchInts];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int* g_scratch_addr[kMaxDevices] = {};
+struct Cached {
+  CUcontext ctx;  // the context the address was looked up in
+  int* addr;
+};
+Cached g_cache[kMaxDevices] = {};
 
-// Device address of g_permute_scratch on the current device (nullptr on error).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_once;
+
+// The driver's current context (nullptr when it cannot be queried).
+CUcontext current_context() {
+  std::call_once(g_ctx_once, []() {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  });
+  CUcontext c = nullptr;
+  if (g_ctx_current == nullptr || g_ctx_current(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of g_permute_scratch in the current device's context, or
+// nullptr with the cause recorded for moe_last_cuda_error().
 int* scratch_address() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const cudaError_t ed = cudaGetDevice(&dev);
+  if (ed != cudaSuccess) {
+    record_cuda_error(ed);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    record_cuda_error(cudaErrorInvalidDevice);
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  // (cudaGetSymbolAddress makes the runtime's context current first: look the
+  // context up after it, so that the pair cached belongs together)
+  const CUcontext before = current_context();
+  Cached& c = g_cache[dev];
+  if (c.addr == nullptr || before == nullptr || c.ctx != before) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
     if (e != cudaSuccess) {
       record_cuda_error(e);
+      c.addr = nullptr;
       return nullptr;
     }
-    g_scratch_addr[dev] = static_cast<int*>(p);
+    c.addr = static_cast<int*>(p);
+    c.ctx = current_context();
   }
-  return g_scratch_addr[dev];
+  return c.addr;
 }
 
 }  // namespace
