@@ -202,7 +202,8 @@ def test_layer_T2048_E896_every_output_and_gradient():
     check_close_chunked("y_perm", layer.y_perm, fwd["y_perm"], chunk=4096)
     bwd = O.layer_backward(inp, fwd)
     check_close("dx", f64(layer.dx), bwd["dx"])
-    check_close("d_w", f64(layer.d_topk_w), bwd["d_w"])
+    # |d_w| reaches ~25 at l = 1024: max-abs relative to max|ref| (like a weight gradient)
+    check_close("d_w", f64(layer.d_topk_w), bwd["d_w"], scale_by_max=True)
     for wn, gn in GRAD_NAMES.items():
         check_close_chunked(gn, layer.grads[wn], bwd[gn], scale_by_max=True)
 
@@ -261,9 +262,12 @@ def test_layer_fwd_bwd_T16384_sampled():
     bwd = O.layer_backward(sub, fwd)
     for name in ("out", "z", "y_lat"):
         check_close(name, f64(getattr(layer, name))[toks], fwd[name])
-    for name in ("dy_lat", "dz", "dx"):
+    for name in ("dz", "dx"):
         check_close(name, f64(getattr(layer, name))[toks], bwd[name])
-    check_close("d_w", f64(layer.d_topk_w)[toks], bwd["d_w"])
+    # internal gradients with values far above 1 (|dy_lat| up to ~8, |d_w| up to
+    # ~25): max-abs relative to max|ref|, like the weight gradients
+    check_close("dy_lat", f64(layer.dy_lat)[toks], bwd["dy_lat"], scale_by_max=True)
+    check_close("d_w", f64(layer.d_topk_w)[toks], bwd["d_w"], scale_by_max=True)
     # sampled experts whose token set is the same on both sides
     touched = set(np.unique(gpu_idx[bad])) | set(np.unique(ref_idx[bad]))
     cand = [e for e in rng.permutation(cfg.E) if e not in touched][:6]
@@ -280,7 +284,7 @@ def test_layer_fwd_bwd_T16384_sampled():
     z_ref = x @ f64(inp["W_dn"])
     dy_ref = g @ f64(inp["W_up"]).T
     check_close("z (all tokens)", f64(layer.z), z_ref)
-    check_close("dy_lat (all tokens)", f64(layer.dy_lat), dy_ref)
+    check_close("dy_lat (all tokens)", f64(layer.dy_lat), dy_ref, scale_by_max=True)
     dz_sh = np.zeros_like(z_ref)
     for s in range(cfg.S):
         dzs, dW13s, dW2s = O.swiglu_expert_backward(z_ref, inp["W13_sh"][s], inp["W2_sh"][s],
