@@ -236,9 +236,9 @@ int moe_grouped_swiglu_ordered(const uint16_t* z_perm, const uint16_t* W13, cons
 /* moe_grouped_swiglu with the permute fused into GEMM1's operand load: the
  * permuted rows are never written. z is the unpermuted latent [T][l] and
  * permuted row r is z[token_of[r]] (token_of from moe_permute, which can then
- * be called with z = NULL); the TMA engine gathers the rows four at a time
- * (tile::gather4) straight into the swizzled shared-memory tile. Results are
- * identical to moe_permute + moe_grouped_swiglu. This is the "less data
+ * be called with z = NULL); warps of the GEMM kernel copy the rows (16-byte
+ * cp.async, z kept in L2) straight into the swizzled shared-memory tile. Results
+ * are identical to moe_permute + moe_grouped_swiglu. This is the "less data
  * movement during token reordering" direction of [OPS]. */
 int moe_grouped_swiglu_gather(const uint16_t* z, const int32_t* token_of, int T,
                               const uint16_t* W13, const uint16_t* W2, const int32_t* offsets,
@@ -295,7 +295,7 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
 
 /* moe_grouped_swiglu_bwd with both permutes fused into the operand loads:
  * dy_perm[r] = dy_lat[token_of[r]] and z_perm[r] = z[token_of[r]] are gathered
- * by TMA inside the dgrad and wgrad GEMMs (dy_lat, z: [T][l]), so neither the
+ * inside the dgrad and wgrad GEMMs (dy_lat, z: [T][l]), so neither the
  * combine backward gather nor the permuted activations are materialised.
  * Results are identical to moe_grouped_swiglu_bwd on the permuted tensors. */
 int moe_grouped_swiglu_bwd_gather(const uint16_t* dy_lat, const uint16_t* z,

@@ -173,16 +173,35 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* map, 
       : "memory");
 }
 
-// Four rows of a 2-D tensor (box of one row) gathered by row index into four
-// consecutive 128-byte rows of shared memory (sm_100 tile::gather4 mode).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, uint64_t* bar, int col,
-                                            int4 rows) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(col), "r"(rows.x), "r"(rows.y),
-      "r"(rows.z), "r"(rows.w)
-      : "memory");
+// ---------------------------------------------------------------- cp.async
+
+// L2 policy that keeps the lines it touches resident in preference to others
+// (for a small source read many times while large tensors stream past it).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16-byte asynchronous copy global -> shared through L2 (the load/store unit's
+// path, not TMA), with an L2 cache policy. Only `src_bytes` (0 or 16) are
+// read; the rest of the 16 bytes is zero-filled.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes,
+                                            uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+               "l"(src), "r"(src_bytes), "l"(policy)
+               : "memory");
+}
+
+// Arrival on `bar` (counted in its expected arrivals) once every cp.async this
+// thread issued before has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // TMA tensor store from shared memory (bulk-group completion).

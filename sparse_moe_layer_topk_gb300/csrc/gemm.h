@@ -81,10 +81,10 @@ struct GemmLaunch {
   // writes C. Deterministic (fixed summation order).
   int splitk = 1;
   float* splitk_ws = nullptr;
-  // Row gather (TMA tile::gather4): with gather_a (gather_b) the A (B) view is
-  // an unpermuted source tensor and permuted row r is its row gather_idx[r].
-  // Supported for the K-major A of a grouped-M GEMM and for one MN-major
-  // operand of a grouped-K GEMM.
+  // Row gather: with gather_a (gather_b) the A (B) view is an unpermuted source
+  // tensor and permuted row r is its row gather_idx[r], copied by extra warps of
+  // the kernel (16-byte cp.async). Supported for the K-major A of a grouped-M
+  // GEMM and for one MN-major operand of a grouped-K GEMM.
   const int* gather_idx = nullptr;
   int gather_a = 0, gather_b = 0;
   // K concatenation (dense, K-major operands): for k >= kcat the A and B tiles

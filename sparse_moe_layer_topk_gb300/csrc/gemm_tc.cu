@@ -8,7 +8,9 @@
 //               tcgen05.mma (M=128, N=BN, K=16) x 4 per stage into a
 //               double-buffered fp32 accumulator in tensor memory.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused elementwise
-//               work (SwiGLU, routing-weight scale, SwiGLU backward), stores.
+//   (or 2..9)   work (SwiGLU, routing-weight scale, SwiGLU backward), stores.
+//   2 more      gathering launches only: copy the gathered operand's rows
+//               (cp.async) into the stage while TMA loads the other operand.
 // The accumulator double buffer lets the epilogue of tile i overlap the
 // mainloop of tile i+1. Ragged expert segments are handled on the device:
 // grouped-M tiles come from the per-expert tile schedule, grouped-K tiles mask
@@ -36,7 +38,9 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int CHUNK_BYTES = 64 * 128;  // one 64-row x 128-byte swizzled block
-constexpr int MISC_BYTES = 768;  // barriers (256 B) + 128 gather row indices (512 B)
+constexpr int MISC_BYTES = 768;  // barriers (256 B) + spare (512 B)
+// Warps that copy a gathered operand's rows (cp.async) in gathering launches.
+constexpr int kGatherWarps = 2;
 
 // BN: tile width (UMMA N); EW: epilogue warps (4, or 8 for heavy epilogues:
 // two warps per TMEM lane quadrant, splitting the tile's column chunks).
@@ -102,9 +106,12 @@ struct Params {
   int* err_flag;
   int c0_rank3;  // the C store map is 3-D (grouped-K groups or column batches)
   // Row gather: permuted row r of the gathered operand is row gather_idx[r] of its
-  // (unpermuted) source tensor, loaded with TMA tile::gather4.
+  // (unpermuted) source tensor, copied by the gather warps (cp.async).
   const int* gather_idx;
   int gather_a, gather_b;
+  const bf16* gsrc;  // the gathered operand's source tensor [rows][gwidth], gld apart
+  long long gld;
+  int gwidth;
   int pair;  // 1: CTA pairs (cluster of 2) own 256-row tiles (dense schedule)
   int mt2;   // pair rows of tiles: ceil(mt / 2)
 };
@@ -249,85 +256,50 @@ __device__ __forceinline__ Tile tile_of(const Params& p, const int4* ttab, int c
 
 // ------------------------------------------------------------------ producer
 
-template <int BN, int EW, bool CW16, bool PAIR, bool WARP>
+template <int BN, int EW, bool CW16, bool PAIR, int GW>
 __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CUtensorMap* mapB,
                               const CUtensorMap* mapA2, const CUtensorMap* mapB2,
-                              uint8_t* smem, uint64_t* full, uint64_t* empty, int* sidx,
-                              const int4* ttab, volatile int* abort_flag) {
-  // WARP: run by the whole warp (the lanes fetch gather indices and issue the
-  // gather4 copies, lane 0 the others); otherwise by lane 0 alone. PAIR: the
-  // CTA loads its own 128 rows of A and its half of the tile's B columns.
+                              uint8_t* smem, uint64_t* full, uint64_t* empty, const int4* ttab,
+                              volatile int* abort_flag) {
+  // Run by one lane. PAIR: the CTA loads its own 128 rows of A and its half of
+  // the tile's B columns. A gathered operand (p.gather_a / p.gather_b) is copied
+  // by the gather warps instead; the stage's expected bytes are then the other
+  // operand's alone.
   using C = Cfg<BN, EW, CW16, PAIR>;
   const int half_n = PAIR ? static_cast<int>(cluster_ctarank()) * (BN / 2) : 0;
-  const uint32_t lane = WARP ? lane_id() : 0u;
   int stage = 0;
   uint32_t phase = 0;
   long long issued = 0;
   const int total = total_tiles(p);
-  const bool gather_m = WARP && p.gather_a && p.sched == SCHED_GROUPED_M;
-  const bool gather_k = WARP && (p.gather_a || p.gather_b) && p.sched == SCHED_GROUPED_K;
+  const bool gather_a = GW > 0 && p.gather_a, gather_b = GW > 0 && p.gather_b;
+  const uint32_t tx_bytes =
+      C::STAGE_BYTES - (gather_a ? A_BYTES : 0) - (gather_b ? C::B_BYTES : 0);
   bool ok = true;
   int it = 0;
   for (int t = tile_begin<PAIR>(); t < total && ok; t += tile_step<PAIR>(), ++it) {
     const Tile ti = tile_of<BN, PAIR>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
-    if (gather_m) {
-      // source rows of the tile's 128 A rows; rows past the expert's segment
-      // repeat its last row (their results are never stored)
-      const int last = ti.m0 + ti.rows - 1;
-      __syncwarp();
-      for (int i = lane; i < BM; i += 32) sidx[i] = __ldg(p.gather_idx + min(ti.m0 + i, last));
-      __syncwarp();
-    }
     for (int kb = 0; kb < ti.nk; ++kb) {
-      int okw = 1;
       // (pairs: the stage is freed by the first CTA's MMA completion, a tcgen05
       // commit multicast to both CTAs)
-      if (lane == 0) okw = mbar_wait<PAIR>(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
-      if (WARP) okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-      if (!okw) {
-        if (lane == 0) raise_abort(abort_flag, p.err_flag);
+      if (!mbar_wait<PAIR>(&empty[stage], phase ^ 1u, abort_flag)) {
+        raise_abort(abort_flag, p.err_flag);
         ok = false;
         break;
       }
       const int k = ti.k0 + kb * BK;
-      if (gather_k) {
-        // source rows of this block's 64 K rows (rows past the segment are zeroed
-        // in shared memory before the MMA; any valid row will do for them)
-        const int last = ti.k0 + ti.krows - 1;
-        __syncwarp();
-        for (int i = lane; i < BK; i += 32) sidx[i] = __ldg(p.gather_idx + min(k + i, last));
-        __syncwarp();
-      }
       const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
       const uint32_t sB = sA + A_BYTES;
-      const int4* gi = reinterpret_cast<const int4*>(sidx);
-      // Gathered operands: each lane issues its own gather4 copies (the
-      // barrier's expected bytes are posted by lane 0; the phase cannot complete
-      // before that arrival, so the order of the two does not matter).
-      if (gather_m) {
-        tma_gather4(sA + lane * 512, mapA, &full[stage], k, gi[lane]);  // 32 groups of 4 rows
-      } else if (gather_k && p.gather_a) {
-        const int c = lane >> 4, g = lane & 15;
-        tma_gather4(sA + c * CHUNK_BYTES + g * 512, mapA, &full[stage], ti.m0 + 64 * c, gi[g]);
-      } else if (gather_k && p.gather_b) {
-#pragma unroll
-        for (int i = 0; i < BN / 128; ++i) {
-          const int cg = lane + 32 * i;
-          const int c = cg >> 4, g = cg & 15;
-          tma_gather4(sB + c * CHUNK_BYTES + g * 512, mapB, &full[stage], ti.nb0 + 64 * c, gi[g]);
-        }
+      int kb_coord = k, batch = ti.batch;
+      if (p.b_batch_mode == BATCH_FROM_K) {
+        batch = k / p.k_per_batch;
+        kb_coord = k - batch * p.k_per_batch;
       }
-      if (PAIR && lane == 0) {
+      if (PAIR) {
         // Both CTAs' copies of the stage count on the first CTA's full barrier,
         // whose producer posts the bytes of both.
         const uint32_t fb = half_n == 0 ? smem_u32(&full[stage])
                                         : cluster_map(smem_u32(&full[stage]), 0);
         if (half_n == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
-        int kb_coord = k, batch = ti.batch;
-        if (p.b_batch_mode == BATCH_FROM_K) {
-          batch = k / p.k_per_batch;
-          kb_coord = k - batch * p.k_per_batch;
-        }
         if (p.kcat > 0 && k >= p.kcat) {
           tma_load_2d_pair(sA, mapA2, fb, k - p.kcat, ti.m0);
           tma_load_2d_pair(sB, mapB2, fb, k - p.kcat, ti.nb0 + half_n);
@@ -352,64 +324,58 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
             else tma_load_3d_pair(sB, mapB, fb, 0, kb_coord, c0);
           }
         }
-      } else if (lane == 0) {
-        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+      } else {
+        mbar_arrive_expect_tx(&full[stage], tx_bytes);
         if (p.kcat > 0 && k >= p.kcat) {
           // second K segment: [A | A2] @ [B ; B2] (both K-major, dense)
           tma_load_2d(sA, mapA2, &full[stage], k - p.kcat, ti.m0);
           tma_load_2d(sB, mapB2, &full[stage], k - p.kcat, ti.nb0);
         } else {
-        // A
-        if (!p.a_mn) {
-          if (!gather_m) tma_load_2d(sA, mapA, &full[stage], k, ti.m0);
-        } else if (!(gather_k && p.gather_a)) {
-          if (p.a_chunked) {
+          // A
+          if (gather_a) {
+            // copied by the gather warps
+          } else if (!p.a_mn) {
+            tma_load_2d(sA, mapA, &full[stage], k, ti.m0);
+          } else if (p.a_chunked) {
             tma_load_3d(sA, mapA, &full[stage], 0, k, ti.m0 >> 6);
           } else {
             tma_load_2d(sA, mapA, &full[stage], ti.m0, k);
             tma_load_2d(sA + CHUNK_BYTES, mapA, &full[stage], ti.m0 + 64, k);
           }
-        }
-        // B
-        int kb_coord = k, batch = ti.batch;
-        if (p.b_batch_mode == BATCH_FROM_K) {
-          batch = k / p.k_per_batch;
-          kb_coord = k - batch * p.k_per_batch;
-        }
-        if (!p.b_mn) {
-          if (p.b_rank3) tma_load_3d(sB, mapB, &full[stage], kb_coord, ti.nb0, batch);
-          else tma_load_2d(sB, mapB, &full[stage], kb_coord, ti.nb0);
-        } else if (p.b_chunked) {
-          // one copy per run of consecutive chunks: the whole tile, or its gate
-          // and up halves (columns nb0 and f + nb0) for the SwiGLU pair
-          const int nruns = p.swiglu_b ? 2 : 1;
-          for (int r = 0; r < nruns; ++r) {
-            const int c0 = (r == 0 ? ti.nb0 : p.f + ti.nb0) >> 6;
-            const uint32_t dst = sB + r * (BN / 2) * 128;
-            if (p.b_rank3) tma_load_4d(dst, mapB, &full[stage], 0, kb_coord, c0, batch);
-            else tma_load_3d(dst, mapB, &full[stage], 0, kb_coord, c0);
-          }
-        } else {
+          // B
+          if (gather_b) {
+            // copied by the gather warps
+          } else if (!p.b_mn) {
+            if (p.b_rank3) tma_load_3d(sB, mapB, &full[stage], kb_coord, ti.nb0, batch);
+            else tma_load_2d(sB, mapB, &full[stage], kb_coord, ti.nb0);
+          } else if (p.b_chunked) {
+            // one copy per run of consecutive chunks: the whole tile, or its gate
+            // and up halves (columns nb0 and f + nb0) for the SwiGLU pair
+            const int nruns = p.swiglu_b ? 2 : 1;
+            for (int r = 0; r < nruns; ++r) {
+              const int c0 = (r == 0 ? ti.nb0 : p.f + ti.nb0) >> 6;
+              const uint32_t dst = sB + r * (BN / 2) * 128;
+              if (p.b_rank3) tma_load_4d(dst, mapB, &full[stage], 0, kb_coord, c0, batch);
+              else tma_load_3d(dst, mapB, &full[stage], 0, kb_coord, c0);
+            }
+          } else {
 #pragma unroll
-          for (int c = 0; c < BN / 64; ++c) {
-            int ncoord;
-            if (p.swiglu_b) {
-              ncoord = (c < BN / 128) ? ti.nb0 + 64 * c : p.f + ti.nb0 + 64 * (c - BN / 128);
-            } else {
-              ncoord = ti.nb0 + 64 * c;
-            }
-            if (gather_k && p.gather_b) {
-              // issued lane-parallel above
-            } else if (p.b_rank3) {
-              tma_load_3d(sB + c * CHUNK_BYTES, mapB, &full[stage], ncoord, kb_coord, batch);
-            } else {
-              tma_load_2d(sB + c * CHUNK_BYTES, mapB, &full[stage], ncoord, kb_coord);
+            for (int c = 0; c < BN / 64; ++c) {
+              int ncoord;
+              if (p.swiglu_b) {
+                ncoord = (c < BN / 128) ? ti.nb0 + 64 * c : p.f + ti.nb0 + 64 * (c - BN / 128);
+              } else {
+                ncoord = ti.nb0 + 64 * c;
+              }
+              if (p.b_rank3) {
+                tma_load_3d(sB + c * CHUNK_BYTES, mapB, &full[stage], ncoord, kb_coord, batch);
+              } else {
+                tma_load_2d(sB + c * CHUNK_BYTES, mapB, &full[stage], ncoord, kb_coord);
+              }
             }
           }
         }
-        }  // first K segment
       }
-      if (WARP) __syncwarp();
       ++issued;
       if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
     }
@@ -417,16 +383,13 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
   if (ok) {
     // Tail: wait until the MMA warp released every stage, so that no
     // tcgen05.commit arrival reaches this CTA's barriers after it exits.
-    if (lane == 0) {
-      for (int i = 0; i < C::STAGES; ++i) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-          raise_abort(abort_flag, p.err_flag);
-          break;
-        }
-        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+    for (int i = 0; i < C::STAGES; ++i) {
+      if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+        raise_abort(abort_flag, p.err_flag);
+        break;
       }
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
     }
-    if (WARP) __syncwarp();
   } else if (!(PAIR && half_n != 0)) {
     // Wait (bounded, ignoring the abort flag) for the copies still in flight so
     // that none lands in shared memory after the CTA exits. (The second CTA of
@@ -442,9 +405,134 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
   }
 }
 
+// ------------------------------------------------------------------ gather warps
+//
+// A gathered operand's row i is row gather_idx[i] of an unpermuted source
+// tensor [rows][gwidth] (row-major bf16, gld elements between rows). GW warps
+// copy each stage's part of it with 16-byte cp.async copies straight into the
+// 128-byte-swizzled layout the MMA reads, and each of their threads arrives on
+// the stage's full barrier once its copies landed. A stage holds ROWS source
+// rows of NCH 64-element chunks each:
+//   grouped-M, K-major A: the tile's 128 rows x one 64-wide K block (NCH = 1);
+//   grouped-K, MN-major A or B: 64 K rows x the tile's 128 (A) or BN (B)
+//   columns, chunk c at c * CHUNK_BYTES (NCH = 2 or BN / 64).
+// Rows past an expert's segment: grouped-M repeats its last row (those rows'
+// results are never stored); grouped-K fills zeros. Chunks past the source
+// width are zero-filled as well.
+template <int GW, int NCH, int ROWS>
+__device__ __forceinline__ void gather_stage(const Params& p, uint32_t dst_base, int gw, int lane,
+                                             const int (&idx)[ROWS / GW / 32 > 0 ? ROWS / GW / 32 : 1],
+                                             int row0_valid_end, int col0, uint64_t pol) {
+  constexpr int PIECES = 8 * NCH;         // 16-byte pieces per row
+  constexpr int RPI = 32 / PIECES;        // rows per warp instruction
+  constexpr int RPW = ROWS / GW;          // rows per warp
+  const int piece = lane % PIECES;
+  const int sub = lane / PIECES;
+  const int c = piece >> 3, q = piece & 7;
+  const bool col_ok = col0 + 64 * c < p.gwidth;
+  const char* src = reinterpret_cast<const char*>(p.gsrc);
+#pragma unroll
+  for (int i = 0; i < RPW / RPI; ++i) {
+    const int ri = RPI * i + sub;               // row within this warp's rows
+    const int r = gw * RPW + ri;                // row within the stage
+    const int srow = __shfl_sync(0xFFFFFFFFu, idx[(RPI * i) >> 5], (RPI * i + sub) & 31);
+    const bool ok = col_ok && r < row0_valid_end;
+    // (a zero-filled piece reads nothing; its address still points into the source)
+    const char* g = src + (static_cast<long long>(srow) * p.gld + (ok ? col0 + 8 * piece : 0)) * 2;
+    const uint32_t d = dst_base + c * CHUNK_BYTES + r * 128 + ((q ^ (r & 7)) << 4);
+    cp_async_16(d, g, ok ? 16u : 0u, pol);
+  }
+}
+
+template <int BN, int EW, bool CW16, int GW>
+__device__ void gather_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                            const int4* ttab, volatile int* abort_flag) {
+  using C = Cfg<BN, EW, CW16>;
+  const int gw = (static_cast<int>(threadIdx.x) >> 5) - 2 - EW;
+  const int lane = static_cast<int>(lane_id());
+  const int total = total_tiles(p);
+  const bool gm = p.sched == SCHED_GROUPED_M;
+  // the gathered source (a few tens of MB, each row read by several experts'
+  // tiles) stays in L2 while the weights and outputs stream past it
+  const uint64_t pol = l2_policy_evict_last();
+  // Source-row indices are fetched one step ahead: grouped-M, the next tile's
+  // rows (this warp's 64 of its 128: lane j holds rows j and 32 + j) while the
+  // current tile is copied; grouped-K, the next K block's 64 rows (this warp's
+  // 32: lane j holds row j) while the current block is copied. Rows past a
+  // segment repeat its last row (grouped-K zero-fills them in the copy).
+  auto rows_m = [&](const Tile& ti, int (&out)[2]) {
+    const int last = ti.m0 + ti.rows - 1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      out[h] = __ldg(p.gather_idx + min(ti.m0 + gw * (BM / GW) + 32 * h + lane, last));
+  };
+  auto rows_k = [&](const Tile& ti, int kb) {
+    const int last = ti.k0 + ti.krows - 1;
+    return __ldg(p.gather_idx + min(ti.k0 + kb * BK + gw * (BK / GW) + lane, last));
+  };
+  int stage = 0;
+  uint32_t phase = 0;
+  int it = 0;
+  int t = tile_begin<false>();
+  Tile ti = tile_of<BN>(p, ttab, C::TT_CAP, 0, t);
+  int idx_m[2] = {0, 0}, nidx_m[2] = {0, 0};
+  int idx_k[1] = {0};
+  if (t < total) {
+    if (gm) rows_m(ti, idx_m);
+    else if (ti.nk > 0) idx_k[0] = rows_k(ti, 0);
+  }
+  bool ok = true;
+  while (t < total && ok) {
+    const int tn = t + tile_step<false>();
+    Tile nt;
+    if (tn < total) {
+      nt = tile_of<BN>(p, ttab, C::TT_CAP, it + 1, tn);
+      if (gm) rows_m(nt, nidx_m);
+    }
+    for (int kb = 0; kb < ti.nk; ++kb) {
+      int okw = 1;
+      if (lane == 0) okw = mbar_wait(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
+      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+      if (!okw) {
+        if (lane == 0) raise_abort(abort_flag, p.err_flag);
+        ok = false;
+        break;
+      }
+      const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
+      if (gm) {
+        // K-major A rows: the tile's 128 rows, K block kb (all rows copied)
+        gather_stage<GW, 1, BM>(p, sA, gw, lane, idx_m, BM, ti.k0 + kb * BK, pol);
+      } else {
+        // grouped-K: this block's 64 K rows; the next block's (or the next
+        // tile's first block's) indices are fetched before these copies issue
+        int nk_idx = 0;
+        if (kb + 1 < ti.nk) nk_idx = rows_k(ti, kb + 1);
+        else if (tn < total && nt.nk > 0) nk_idx = rows_k(nt, 0);
+        const int valid = ti.krows - kb * BK;
+        if (p.gather_a)
+          gather_stage<GW, BM / 64, BK>(p, sA, gw, lane, idx_k, valid, ti.m0, pol);
+        else
+          gather_stage<GW, BN / 64, BK>(p, sA + A_BYTES, gw, lane, idx_k, valid, ti.nb0, pol);
+        idx_k[0] = nk_idx;
+      }
+      cp_async_arrive_noinc(&full[stage]);
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+    }
+    if (!ok) break;
+    if (!gm && ti.nk == 0 && tn < total && nt.nk > 0) idx_k[0] = rows_k(nt, 0);
+    ti = nt;
+    idx_m[0] = nidx_m[0];
+    idx_m[1] = nidx_m[1];
+    t = tn;
+    ++it;
+  }
+  // nothing may land in shared memory after the CTA exits
+  cp_async_wait_all();
+}
+
 // ------------------------------------------------------------------ MMA
 
-template <int BN, int EW, bool CW16>
+template <int BN, int EW, bool CW16, int GW>
 __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                          uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
                          const int4* ttab, volatile int* abort_flag) {
@@ -476,6 +564,8 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
         break;
       }
       tc_fence_after();
+      // rows the gather warps copied (generic proxy) are read by the MMA (async proxy)
+      if constexpr (GW > 0) fence_proxy_async_smem();
       uint8_t* sA = smem + stage * C::STAGE_BYTES;
       int nkk = BK / 16;  // K=16 MMAs of this block
       if (p.sched == SCHED_GROUPED_K) {
@@ -1126,8 +1216,8 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   __syncwarp();
 }
 
-template <int BN, int EW, bool CW16, bool PAIR>
-__global__ void __launch_bounds__(64 + 32 * EW, 1)
+template <int BN, int EW, bool CW16, bool PAIR, int GW>
+__global__ void __launch_bounds__(64 + 32 * (EW + GW), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC0,
@@ -1146,10 +1236,9 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* sidx = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 256);  // 128 gather indices
   int4* ttab = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(full) + MISC_BYTES);
   const int warp = threadIdx.x >> 5;
-  if (p.sched != SCHED_DENSE && warp >= 2) {
+  if (p.sched != SCHED_DENSE && warp >= 2 && warp < 2 + EW) {
     // the epilogue warps decode this CTA's first TT_CAP tiles in parallel
     const int total = total_tiles(p);
     const int mine = total > static_cast<int>(blockIdx.x)
@@ -1161,8 +1250,10 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   }
 
   if (threadIdx.x == 0) {
+    // a stage is full once the producer posted its TMA bytes (one arrival) and,
+    // in gathering launches, every gather thread's copies landed
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + 32 * GW);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -1191,26 +1282,24 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // Gathering launches run the producer on the whole warp (the lanes fetch
-    // indices and issue gather4 copies); the others on lane 0 alone.
-    if (!PAIR && (p.gather_a || p.gather_b))
-      producer_loop<BN, EW, CW16, PAIR, true>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty,
-                                              sidx, ttab, abort_flag);
-    else if (lane_id() == 0)
-      producer_loop<BN, EW, CW16, PAIR, false>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty,
-                                               sidx, ttab, abort_flag);
+    if (lane_id() == 0)
+      producer_loop<BN, EW, CW16, PAIR, GW>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty,
+                                            ttab, abort_flag);
   } else if (warp == 1) {
     if constexpr (!PAIR) {
-      mma_loop<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base, ttab,
-                             abort_flag);
+      mma_loop<BN, EW, CW16, GW>(p, smem, full, empty, tfull, tempty, drain, tmem_base, ttab,
+                                 abort_flag);
     } else {
       if (cluster_ctarank() == 0)  // the second CTA's MMA warp has nothing to do
         mma_loop_pair<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base,
                                     abort_flag);
     }
-  } else {
+  } else if (warp < 2 + EW) {
     const StoreMaps sm{&mapC0, &mapC1, p.c0_rank3};
     epilogue_loop<BN, EW, CW16, PAIR>(p, sm, staging, tfull, tempty, tmem_base, ttab, abort_flag);
+  } else {
+    if constexpr (GW > 0 && !PAIR) gather_loop<BN, EW, CW16, GW>(p, smem, full, empty, ttab,
+                                                                 abort_flag);
   }
   tc_fence_before();
   if (PAIR) cluster_sync_all();  // no CTA frees tensor memory the pair's MMAs may still use
@@ -1299,9 +1388,10 @@ bool make_store_map(CUtensorMap* map, void* ptr, bool f32, bool rank3, long long
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int EW, bool CW16, bool PAIR>
+template <int BN, int EW, bool CW16, bool PAIR, int GW = 0>
 int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   using C = Cfg<BN, EW, CW16, PAIR>;
+  constexpr int THREADS = C::THREADS + 32 * GW;
   Params p{};
   p.pair = PAIR ? 1 : 0;
   p.sched = L.sched;
@@ -1360,6 +1450,13 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   p.gather_idx = L.gather_idx;
   p.gather_a = L.gather_a;
   p.gather_b = L.gather_b;
+  if ((L.gather_a || L.gather_b) != (GW > 0)) return MOE_ERR_UNSUPPORTED;
+  if (L.gather_a || L.gather_b) {
+    const MatView& g = L.gather_a ? L.A : L.B;
+    p.gsrc = reinterpret_cast<const bf16*>(g.ptr);
+    p.gld = g.ld;
+    p.gwidth = static_cast<int>(g.cols);
+  }
   if (L.gather_a || L.gather_b) {
     // supported: K-major A of a grouped-M GEMM, MN-major A or B of a grouped-K GEMM
     const bool okm = L.sched == SCHED_GROUPED_M && L.gather_a && !L.gather_b && !L.a_mn;
@@ -1386,9 +1483,10 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
       return MOE_ERR_ARG;
     p.kcat = L.kcat;
   }
-  // gathered operands are read one row per box (tile::gather4); other MN-major
-  // operands through a chunked map when their columns allow (else one copy per
-  // 64-column chunk)
+  // (a gathered operand is copied by the gather warps, not by TMA: its map is
+  // encoded only so that every map the kernel receives is a valid one.) Other
+  // MN-major operands are read through a chunked map when their columns allow
+  // (else one copy per 64-column chunk)
   // (the chunk coordinate is m0 / 64: grouped-M row starts are not 64-aligned)
   p.a_chunked = L.a_mn && !L.gather_a && L.sched != SCHED_GROUPED_M &&
                 make_map_chunked(&mapA, L.A, BM / 64, false);
@@ -1443,7 +1541,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EW, CW16, PAIR>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EW, CW16, PAIR, GW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) {
@@ -1470,12 +1568,12 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     LaunchTimer lt(L.name, stream);
-    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EW, CW16, PAIR>, mapA, mapB, mapC0, mapC1,
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EW, CW16, PAIR, GW>, mapA, mapB, mapC0, mapC1,
                            mapA2, mapB2, p);
   } else {
     const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
     LaunchTimer lt(L.name, stream);
-    gemm_tc_kernel<BN, EW, CW16, PAIR><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
+    gemm_tc_kernel<BN, EW, CW16, PAIR, GW><<<grid, THREADS, C::SMEM_BYTES, stream>>>(
         mapA, mapB, mapC0, mapC1, mapA2, mapB2, p);
     e = cudaSuccess;
   }
@@ -1539,13 +1637,22 @@ int gemm_launch(const GemmLaunch& L, cudaStream_t stream) {
   const bool cw16 = L.epi == EPI_SWIGLU;
   // CTA pairs (256-row tiles, cta_group::2 MMAs, half of B per CTA) for the dense
   // schedule with 256-wide tiles and at least two row blocks
+  const bool gather = L.gather_a || L.gather_b;
   const bool pair = L.pair && L.BN == 256 && L.sched == SCHED_DENSE && L.K > 0 && L.M > BM &&
-                    !L.gather_a && !L.gather_b;
+                    !gather;
   int st;
   if (L.BN == 256 && pair)
     st = ew == 4 ? launch_bn<256, 4, false, true>(L, stream)
                  : (cw16 ? launch_bn<256, 8, true, true>(L, stream)
                          : launch_bn<256, 8, false, true>(L, stream));
+  else if (gather && L.BN == 256)
+    st = ew == 4 ? launch_bn<256, 4, false, false, kGatherWarps>(L, stream)
+                 : (cw16 ? launch_bn<256, 8, true, false, kGatherWarps>(L, stream)
+                         : launch_bn<256, 8, false, false, kGatherWarps>(L, stream));
+  else if (gather && L.BN == 128)
+    st = ew == 4 ? launch_bn<128, 4, false, false, kGatherWarps>(L, stream)
+                 : (cw16 ? launch_bn<128, 8, true, false, kGatherWarps>(L, stream)
+                         : launch_bn<128, 8, false, false, kGatherWarps>(L, stream));
   else if (L.BN == 256)
     st = ew == 4 ? launch_bn<256, 4, false, false>(L, stream)
                  : (cw16 ? launch_bn<256, 8, true, false>(L, stream)

@@ -13,9 +13,9 @@ Backward (dout given): latent_proj_bwd(up) -> unpermute_combine_bwd ->
 With fused_gather the permute only builds the maps and the grouped GEMMs
 gather their permuted rows from z and dy_lat themselves
 (moe_grouped_swiglu[_bwd]_gather): z_perm and dy_perm are never written. It
-saves ~1 GB of activations at T=16384 but is slower on GB300 (the TMA gather4
-row loads run at a fraction of the tiled loads' rate), so the default is the
-explicit permute.
+saves ~1 GB of activations and ~2 GB of DRAM traffic at T=16384 but is slower
+on GB300 (the row copies keep fewer bytes in flight per SM than the tiled TMA
+loads of the permuted tensors), so the default is the explicit permute.
 """
 from __future__ import annotations
 
