@@ -46,13 +46,16 @@ constexpr int kGatherWarps = 2;
 // two warps per TMEM lane quadrant, splitting the tile's column chunks).
 // PAIR: the CTA is one of a pair computing 256-row tiles with cta_group::2 MMAs
 // (each CTA holds its 128 rows of A and half of B's columns).
-template <int BN, int EW, bool CW16 = false, bool PAIR = false>
+// SBWD: the SwiGLU-backward epilogue with TMA-staged inputs (4 warps, each
+// with three 6 KB slots for a chunk's g, u and h blocks).
+template <int BN, int EW, bool CW16 = false, bool PAIR = false, bool SBWD = false>
 struct Cfg {
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES =
-      PAIR ? ((EW == 8 && !CW16) ? 5 : 6)
-           : ((BN == 256) ? ((EW == 8 && !CW16) ? 3 : 4) : ((EW == 8 && !CW16) ? 5 : 6));
+      SBWD ? ((BN == 256 && !PAIR) ? 3 : 4)
+           : PAIR ? ((EW == 8 && !CW16) ? 5 : 6)
+                  : ((BN == 256) ? ((EW == 8 && !CW16) ? 3 : 4) : ((EW == 8 && !CW16) ? 5 : 6));
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int THREADS = 64 + 32 * EW;
   // Per-warp output staging, a ring of slots of one chunk's output each (4 KB
@@ -61,7 +64,7 @@ struct Cfg {
   // the next chunks are staged: one fp32 / three bf16 slots with 4 epilogue
   // warps (a whole tile table of a ragged-K weight gradient measured faster
   // than a second fp32 slot), one SwiGLU chunk with 8.
-  static constexpr int STG = CW16 ? 3072 : (EW == 8 ? 6144 : 7168);
+  static constexpr int STG = SBWD ? 3 * 6144 : (CW16 ? 3072 : (EW == 8 ? 6144 : 7168));
   // The rest of the 227 KB (after 1 KB alignment slack and the barriers) holds
   // the CTA's table of decoded grouped tiles, 16 bytes per tile.
   static constexpr int SMEM_LIMIT = 232448;
@@ -112,6 +115,7 @@ struct Params {
   const bf16* gsrc;  // the gathered operand's source tensor [rows][gwidth], gld apart
   long long gld;
   int gwidth;
+  int tt_cap;  // tiles of a CTA held in its shared-memory table (the rest are decoded inline)
   int pair;  // 1: CTA pairs (cluster of 2) own 256-row tiles (dense schedule)
   int mt2;   // pair rows of tiles: ceil(mt / 2)
 };
@@ -227,8 +231,8 @@ __device__ __forceinline__ int4 pack_tile(const Params& p, const Tile& ti) {
 // The i-th tile (t = blockIdx.x + i * gridDim.x) of this CTA: from the table when
 // it holds it (the first `cap` tiles), else decoded from the schedule.
 template <int BN, bool PAIR = false>
-__device__ __forceinline__ Tile tile_of(const Params& p, const int4* ttab, int cap, int i, int t) {
-  if (p.sched == SCHED_DENSE || i >= cap) return decode<BN, PAIR>(p, t);
+__device__ __forceinline__ Tile tile_of(const Params& p, const int4* ttab, int i, int t) {
+  if (p.sched == SCHED_DENSE || i >= p.tt_cap) return decode<BN, PAIR>(p, t);
   const int4 e = ttab[i];
   const int bn_eff = p.swiglu_b ? BN / 2 : BN;
   Tile ti;
@@ -256,7 +260,7 @@ __device__ __forceinline__ Tile tile_of(const Params& p, const int4* ttab, int c
 
 // ------------------------------------------------------------------ producer
 
-template <int BN, int EW, bool CW16, bool PAIR, int GW>
+template <int BN, int EW, bool CW16, bool PAIR, int GW, bool SBWD>
 __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CUtensorMap* mapB,
                               const CUtensorMap* mapA2, const CUtensorMap* mapB2,
                               uint8_t* smem, uint64_t* full, uint64_t* empty, const int4* ttab,
@@ -265,7 +269,7 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
   // the tile's B columns. A gathered operand (p.gather_a / p.gather_b) is copied
   // by the gather warps instead; the stage's expected bytes are then the other
   // operand's alone.
-  using C = Cfg<BN, EW, CW16, PAIR>;
+  using C = Cfg<BN, EW, CW16, PAIR, SBWD>;
   const int half_n = PAIR ? static_cast<int>(cluster_ctarank()) * (BN / 2) : 0;
   int stage = 0;
   uint32_t phase = 0;
@@ -277,7 +281,7 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
   bool ok = true;
   int it = 0;
   for (int t = tile_begin<PAIR>(); t < total && ok; t += tile_step<PAIR>(), ++it) {
-    const Tile ti = tile_of<BN, PAIR>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
+    const Tile ti = tile_of<BN, PAIR>(p, ttab, it, t);
     for (int kb = 0; kb < ti.nk; ++kb) {
       // (pairs: the stage is freed by the first CTA's MMA completion, a tcgen05
       // commit multicast to both CTAs)
@@ -444,10 +448,10 @@ __device__ __forceinline__ void gather_stage(const Params& p, uint32_t dst_base,
   }
 }
 
-template <int BN, int EW, bool CW16, int GW>
+template <int BN, int EW, bool CW16, int GW, bool SBWD>
 __device__ void gather_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                             const int4* ttab, volatile int* abort_flag) {
-  using C = Cfg<BN, EW, CW16>;
+  using C = Cfg<BN, EW, CW16, false, SBWD>;
   const int gw = (static_cast<int>(threadIdx.x) >> 5) - 2 - EW;
   const int lane = static_cast<int>(lane_id());
   const int total = total_tiles(p);
@@ -474,7 +478,7 @@ __device__ void gather_loop(const Params& p, uint8_t* smem, uint64_t* full, uint
   uint32_t phase = 0;
   int it = 0;
   int t = tile_begin<false>();
-  Tile ti = tile_of<BN>(p, ttab, C::TT_CAP, 0, t);
+  Tile ti = tile_of<BN>(p, ttab, 0, t);
   int idx_m[2] = {0, 0}, nidx_m[2] = {0, 0};
   int idx_k[1] = {0};
   if (t < total) {
@@ -486,7 +490,7 @@ __device__ void gather_loop(const Params& p, uint8_t* smem, uint64_t* full, uint
     const int tn = t + tile_step<false>();
     Tile nt;
     if (tn < total) {
-      nt = tile_of<BN>(p, ttab, C::TT_CAP, it + 1, tn);
+      nt = tile_of<BN>(p, ttab, it + 1, tn);
       if (gm) rows_m(nt, nidx_m);
     }
     for (int kb = 0; kb < ti.nk; ++kb) {
@@ -532,11 +536,11 @@ __device__ void gather_loop(const Params& p, uint8_t* smem, uint64_t* full, uint
 
 // ------------------------------------------------------------------ MMA
 
-template <int BN, int EW, bool CW16, int GW>
+template <int BN, int EW, bool CW16, int GW, bool SBWD>
 __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                          uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
                          const int4* ttab, volatile int* abort_flag) {
-  using C = Cfg<BN, EW, CW16>;
+  using C = Cfg<BN, EW, CW16, false, SBWD>;
   const uint32_t lane = lane_id();
   const uint32_t idesc = make_idesc_bf16(BM, BN, p.a_mn, p.b_mn);
   const uint32_t a_lbo = p.a_mn ? CHUNK_BYTES : 16, b_lbo = p.b_mn ? CHUNK_BYTES : 16;
@@ -548,7 +552,7 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   int it = 0;
   bool ok = true;
   for (int t = tile_begin<false>(); t < total && ok; t += tile_step<false>(), ++it) {
-    const Tile ti = tile_of<BN>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
+    const Tile ti = tile_of<BN>(p, ttab, it, t);
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
     if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
@@ -629,10 +633,10 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
 // the stage in both CTAs and, per tile, fills both CTAs' accumulators
 // (multicast commits). The accumulator buffer is free once the epilogue warps
 // of both CTAs released it (tempty, 2 * EW arrivals).
-template <int BN, int EW, bool CW16>
+template <int BN, int EW, bool CW16, bool SBWD>
 __device__ void mma_loop_pair(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* tfull, uint64_t* tempty, uint64_t* drain,
                               uint32_t tmem_base, volatile int* abort_flag) {
-  using C = Cfg<BN, EW, CW16, true>;
+  using C = Cfg<BN, EW, CW16, true, SBWD>;
   const uint32_t lane = lane_id();
   const uint32_t idesc = make_idesc_bf16(2 * BM, BN, p.a_mn, p.b_mn);
   const uint32_t a_lbo = p.a_mn ? CHUNK_BYTES : 16, b_lbo = p.b_mn ? CHUNK_BYTES : 16;
@@ -778,7 +782,210 @@ struct StoreMaps {
   const CUtensorMap* c0;  // C / h / dgu
   const CUtensorMap* c1;  // gu (SwiGLU) / w*h (SwiGLU backward)
   int c0_rank3;
+  const CUtensorMap* ld_gu;  // SwiGLU backward: load maps of the saved g|u and h
+  const CUtensorMap* ld_h;
 };
+
+// SwiGLU-backward element math for eight columns: dh = w * acc,
+// dg = dh * u * s(g) * (1 + g (1 - s(g))), du = dh * silu(g), the routing-weight
+// dot acc . h, and w * h (the dW2 operand); bf16 in and out, fp32 math.
+__device__ __forceinline__ void swiglu_bwd8(const float* a, uint4 G, uint4 U, uint4 H, float w,
+                                            float& dot, uint4& DG, uint4& DU, uint4& HW) {
+  const uint32_t Gw[4] = {G.x, G.y, G.z, G.w};
+  const uint32_t Uw[4] = {U.x, U.y, U.z, U.w};
+  const uint32_t Hw[4] = {H.x, H.y, H.z, H.w};
+  uint32_t pdg[4], pdu[4], phw[4];
+#pragma unroll
+  for (int e2 = 0; e2 < 4; ++e2) {
+    float dgv[2], duv[2], hwv[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float av = a[2 * e2 + hh];
+      const float gg = hh ? bf16_hi(Gw[e2]) : bf16_lo(Gw[e2]);
+      const float uu = hh ? bf16_hi(Uw[e2]) : bf16_lo(Uw[e2]);
+      const float hv = hh ? bf16_hi(Hw[e2]) : bf16_lo(Hw[e2]);
+      const float sg = sigmoidf_(gg);
+      const float dh = w * av;
+      dgv[hh] = dh * uu * sg * (1.0f + gg * (1.0f - sg));
+      duv[hh] = dh * gg * sg;
+      dot = fmaf(av, hv, dot);
+      hwv[hh] = w * hv;
+    }
+    pdg[e2] = pack_bf16(dgv[0], dgv[1]);
+    pdu[e2] = pack_bf16(duv[0], duv[1]);
+    phw[e2] = pack_bf16(hwv[0], hwv[1]);
+  }
+  DG = make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]);
+  DU = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
+  HW = make_uint4(phw[0], phw[1], phw[2], phw[3]);
+}
+
+// SwiGLU-backward epilogue with TMA-staged inputs. Each of the 4 epilogue
+// warps owns the 32 accumulator rows of its tensor-memory lane quadrant and a
+// ring of three 6 KB slots in shared memory; a slot holds the g, u and h blocks
+// (32 rows x 32 columns, bf16, 64-byte rows with 64-byte swizzle) of one
+// 32-column chunk. Lane 0 loads them by TMA two chunks ahead of the chunk being
+// computed (across tile boundaries too). The chunk's dg, du and w*h overwrite g,
+// u and h in place and leave by TMA store from the same slot. (Loading the
+// inputs lane by lane instead makes every load instruction touch 32 rows, so
+// the L1's request rate, not DRAM, sets the pace.)
+template <int BN, bool PAIR>
+__device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t* staging,
+                                   uint64_t* lbar, uint64_t* tfull, uint64_t* tempty,
+                                   uint32_t tmem_base, const int4* ttab, volatile int* abort_flag) {
+  using C = Cfg<BN, 4, false, PAIR, true>;
+  constexpr int SLOT = 6144;
+  constexpr int NCH = BN / 32;
+  const int warp = static_cast<int>(threadIdx.x) >> 5;
+  const int q = warp & 3;
+  const int ew = warp - 2;
+  const uint32_t lane = lane_id();
+  uint8_t* const slots = staging + ew * C::STG;
+  uint64_t* const lb = lbar + 3 * ew;
+  const int total = total_tiles(p);
+  const int sw = (static_cast<int>(lane) >> 1) & 3;  // 64-byte swizzle of this lane's row
+
+  // The jobs (tile, chunk) this warp computes, in order, walked ahead of the
+  // computation to request their inputs: tiles with rows in this warp's
+  // quadrant, chunks inside N.
+  int a_it = 0, a_t = tile_begin<PAIR>(), a_c = 0;
+  Tile a_ti;
+  bool a_have = false;
+  auto a_seek = [&]() -> bool {
+    while (a_t < total) {
+      if (!a_have) {
+        a_ti = tile_of<BN, PAIR>(p, ttab, a_it, a_t);
+        a_have = true;
+      }
+      if (a_ti.rows - q * 32 > 0 && a_c < NCH && a_ti.nb0 + 32 * a_c < p.N) return true;
+      a_c = 0;
+      a_t += tile_step<PAIR>();
+      ++a_it;
+      a_have = false;
+    }
+    return false;
+  };
+  long long issued = 0;  // jobs whose inputs were requested
+  auto issue = [&]() {
+    const int n = a_ti.nb0 + 32 * a_c;
+    const int sx = n / p.f;
+    const int gcol = sx * 2 * p.f + (n - sx * p.f);
+    const int row0 = a_ti.m0 + q * 32;
+    const int slot = static_cast<int>(issued % 3);
+    if (lane == 0) {
+      const uint32_t d = smem_u32(slots + slot * SLOT);
+      mbar_arrive_expect_tx(&lb[slot], SLOT);
+      tma_load_2d(d, sm.ld_gu, &lb[slot], gcol, row0);
+      tma_load_2d(d + 2048, sm.ld_gu, &lb[slot], gcol + p.f, row0);
+      tma_load_2d(d + 4096, sm.ld_h, &lb[slot], n, row0);
+    }
+    ++issued;
+    ++a_c;
+  };
+  for (int i = 0; i < 2 && a_seek(); ++i) issue();
+
+  long long done = 0;  // jobs computed
+  bool ok = true;
+  int it = 0;
+  for (int t = tile_begin<PAIR>(); t < total && ok; t += tile_step<PAIR>(), ++it) {
+    const Tile ti = tile_of<BN, PAIR>(p, ttab, it, t);
+    const int buf = it & 1;
+    const uint32_t use = static_cast<uint32_t>(it >> 1);
+    if (!mbar_wait<PAIR>(&tfull[buf], use & 1u, abort_flag)) {
+      raise_abort(abort_flag, p.err_flag);
+      break;
+    }
+    tc_fence_after();
+    const int blk_rows = ti.rows - q * 32;
+    const int r_loc = q * 32 + static_cast<int>(lane);
+    const bool row_ok = r_loc < ti.rows;
+    const long long grow = static_cast<long long>(ti.m0) + r_loc;
+    const int row0 = ti.m0 + q * 32;
+    const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(buf * BN);
+    // TMA clips outside the tensor; inside it (grouped-M) only full blocks may use it
+    const bool use_tma = blk_rows >= 32 || p.sched != SCHED_GROUPED_M;
+    if (blk_rows > 0) {
+      const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
+      float dot = 0.0f;
+      for (int c = 0; c < NCH; ++c) {
+        const int n = ti.nb0 + c * 32;
+        if (n >= p.N) break;
+        const int slot = static_cast<int>(done % 3);
+        int okw = 1;
+        if (lane == 0)
+          okw = mbar_wait(&lb[slot], static_cast<uint32_t>((done / 3) & 1), abort_flag) ? 1 : 0;
+        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+        if (!okw) {
+          if (lane == 0) raise_abort(abort_flag, p.err_flag);
+          ok = false;
+          break;
+        }
+        float a[32];
+        ld_chunk(trow + c * 32, a);
+        const int sx = n / p.f;
+        const int gcol = sx * 2 * p.f + (n - sx * p.f);
+        uint8_t* const sl = slots + slot * SLOT;
+        uint8_t* const rowp = sl + lane * 64;
+        bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + gcol;
+#pragma unroll
+        for (int vv = 0; vv < 4; ++vv) {
+          const int off = (vv ^ sw) << 4;
+          uint4 DG, DU, HW;
+          swiglu_bwd8(a + 8 * vv, *reinterpret_cast<const uint4*>(rowp + off),
+                      *reinterpret_cast<const uint4*>(rowp + 2048 + off),
+                      *reinterpret_cast<const uint4*>(rowp + 4096 + off), w, dot, DG, DU, HW);
+          if (use_tma) {
+            *reinterpret_cast<uint4*>(rowp + off) = DG;
+            *reinterpret_cast<uint4*>(rowp + 2048 + off) = DU;
+            *reinterpret_cast<uint4*>(rowp + 4096 + off) = HW;
+          } else if (row_ok) {
+            store16(dgdst + vv * 8, DG);
+            store16(dgdst + p.f + vv * 8, DU);
+            if (p.aux) store16(p.aux + grow * p.ldaux + n + vv * 8, HW);
+          }
+        }
+        if (use_tma) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t src = smem_u32(sl);
+            tma_store_2d(sm.c0, src, gcol, row0);
+            tma_store_2d(sm.c0, src + 2048, gcol + p.f, row0);
+            if (p.aux) tma_store_2d(sm.c1, src + 4096, n, row0);
+            bulk_commit();
+          }
+        }
+        ++done;
+        // the next request reuses the slot of the job before this one: its
+        // stores (committed before this job's) must have read it
+        if (a_seek()) {
+          __syncwarp();
+          if (lane == 0) bulk_wait_read_max(use_tma ? 1 : 0);
+          __syncwarp();
+          issue();
+        }
+      }
+      if (ok && row_ok && p.dw_part) p.dw_part[grow * p.dw_nparts + ti.n_blk] = dot;
+    }
+    tc_fence_before();
+    if (PAIR) {
+      // one arrival per warp on the pair's first CTA (it issues the MMAs)
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&tempty[buf]), 0));
+    } else {
+      mbar_arrive(&tempty[buf]);
+    }
+  }
+  // inputs requested but never computed (after an abort) land before the CTA exits
+  if (lane == 0) {
+    volatile int never = 0;
+    for (long long j = done; j < issued; ++j)
+      mbar_wait(&lb[j % 3], static_cast<uint32_t>((j / 3) & 1), &never);
+    bulk_wait_all();
+  }
+  __syncwarp();
+}
 
 template <int BN, int EW, bool CW16, bool PAIR>
 __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* staging,
@@ -795,8 +1002,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   int slot_bytes;
   if (p.epi == EPI_STORE) slot_bytes = p.c_bf16 ? 2048 : 4096;
   else if (p.epi == EPI_ROWSCALE) slot_bytes = 2048;
-  else if (p.epi == EPI_SWIGLU) slot_bytes = (CW16 ? 1024 : 2048) * (p.gu ? 3 : 1);
-  else slot_bytes = (CW16 ? 1024 : 2048) * (p.aux ? 3 : 2);
+  else slot_bytes = (CW16 ? 1024 : 2048) * (p.gu ? 3 : 1);  // EPI_SWIGLU
   int nslots = Cfg<BN, EW, CW16>::STG / slot_bytes;
   if (nslots > 4) nslots = 4;
   int slot = 0;
@@ -819,12 +1025,8 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
     __syncwarp();
   };
   int it = 0;
-  // SwiGLU backward: g and u of the warp's first chunk of a tile, loaded during
-  // the last chunk of the tile before (they are inputs, not accumulator data)
-  uint4 Gn[4], Un[4];
-  bool gu_ready = false;
   for (int t = tile_begin<PAIR>(); t < total; t += tile_step<PAIR>(), ++it) {
-    const Tile ti = tile_of<BN, PAIR>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it, t);
+    const Tile ti = tile_of<BN, PAIR>(p, ttab, it, t);
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
     if (!mbar_wait<PAIR>(&tfull[buf], use & 1u, abort_flag)) {
@@ -996,211 +1198,6 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             store_bf16_row(reinterpret_cast<bf16*>(p.C) + grow * p.ldc + n, v);
           }
         }
-      } else {  // EPI_SWIGLU_BWD
-        if constexpr (CW16) {
-        const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
-        float dot = 0.0f;
-        // 16-column chunks; g and u of the warp's next chunk are loaded one chunk
-        // ahead, h of the current chunk at its start (it is needed last).
-        uint4 Gn[2], Un[2];
-        auto load_gu = [&](int n, uint4* G, uint4* U) {
-          const int s = n / p.f;
-          const bf16* gsrc = p.gu + grow * p.ldgu + s * 2 * p.f + (n - s * p.f);
-#pragma unroll
-          for (int vv = 0; vv < 2; ++vv) {
-            G[vv] = *reinterpret_cast<const uint4*>(gsrc + vv * 8);
-            U[vv] = *reinterpret_cast<const uint4*>(gsrc + p.f + vv * 8);
-          }
-        };
-        const uint4 z4 = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int vv = 0; vv < 2; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
-        if (row_ok && ti.nb0 + grp * 16 < p.N) load_gu(ti.nb0 + grp * 16, Gn, Un);
-        const int sw = (lane >> 2) & 1;  // 32-byte swizzle of this lane's staging row
-#pragma unroll 1
-        for (int c = grp; c < BN / 16; c += NG) {
-          const int n = ti.nb0 + c * 16;  // column of dh within [0, S*f)
-          if (n >= p.N) break;
-          uint4 Gc[2], Uc[2], Hc[2];
-#pragma unroll
-          for (int vv = 0; vv < 2; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; Hc[vv] = z4; }
-          if (row_ok) {
-            const bf16* hsrc = p.h + grow * p.ldh + n;
-#pragma unroll
-            for (int vv = 0; vv < 2; ++vv) Hc[vv] = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
-            if (c + NG < BN / 16 && n + 16 * NG < p.N) load_gu(n + 16 * NG, Gn, Un);
-          }
-          float a[16];
-          ld_chunk16(trow + c * 16, a);
-          const int s = n / p.f;
-          const int jj = n - s * p.f;
-          const int gcol = s * 2 * p.f + jj;
-          if (use_tma) stage_begin();
-          bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + gcol;
-#pragma unroll
-          for (int vv = 0; vv < 2; ++vv) {
-            const uint32_t Gw[4] = {Gc[vv].x, Gc[vv].y, Gc[vv].z, Gc[vv].w};
-            const uint32_t Uw[4] = {Uc[vv].x, Uc[vv].y, Uc[vv].z, Uc[vv].w};
-            const uint32_t Hw[4] = {Hc[vv].x, Hc[vv].y, Hc[vv].z, Hc[vv].w};
-            uint32_t pdg[4], pdu[4], phw[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              float dgv[2], duv[2], hwv[2];
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const float av = a[vv * 8 + 2 * e2 + hh];
-                const float gg = hh ? bf16_hi(Gw[e2]) : bf16_lo(Gw[e2]);
-                const float uu = hh ? bf16_hi(Uw[e2]) : bf16_lo(Uw[e2]);
-                const float hv = hh ? bf16_hi(Hw[e2]) : bf16_lo(Hw[e2]);
-                const float sg = sigmoidf_(gg);
-                const float dh = w * av;
-                dgv[hh] = dh * uu * sg * (1.0f + gg * (1.0f - sg));
-                duv[hh] = dh * gg * sg;
-                dot = fmaf(av, hv, dot);
-                hwv[hh] = w * hv;
-              }
-              pdg[e2] = pack_bf16(dgv[0], dgv[1]);
-              pdu[e2] = pack_bf16(duv[0], duv[1]);
-              phw[e2] = pack_bf16(hwv[0], hwv[1]);
-            }
-            const uint4 DG = make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]);
-            const uint4 DU = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
-            const uint4 HW = make_uint4(phw[0], phw[1], phw[2], phw[3]);
-            if (use_tma) {
-              const int off = lane * 32 + ((vv ^ sw) << 4);
-              *reinterpret_cast<uint4*>(stg + off) = DG;
-              *reinterpret_cast<uint4*>(stg + 1024 + off) = DU;
-              if (p.aux) *reinterpret_cast<uint4*>(stg + 2048 + off) = HW;
-            } else if (row_ok) {
-              store16(dgdst + vv * 8, DG);
-              store16(dgdst + p.f + vv * 8, DU);
-              if (p.aux) store16(p.aux + grow * p.ldaux + n + vv * 8, HW);
-            }
-          }
-          if (use_tma) {
-            stage_end();
-            if (lane == 0) {
-              tma_store_2d(sm.c0, stg_s, gcol, row0);
-              tma_store_2d(sm.c0, stg_s + 1024, gcol + p.f, row0);
-              if (p.aux) tma_store_2d(sm.c1, stg_s + 2048, n, row0);
-              bulk_commit();
-            }
-            pending = true;
-          }
-        }
-        if (row_ok && p.dw_part) p.dw_part[grow * p.dw_nparts + ti.n_blk * NG + grp] = dot;
-        } else {
-        const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
-        float dot = 0.0f;
-        // g and u of the next chunk are loaded one chunk ahead (across tiles too),
-        // h of the current chunk at its start (it is needed last); results go to
-        // the staging blocks 8 columns at a time to keep the register footprint small.
-        auto load_gu = [&](long long row, int n, uint4* G, uint4* U) {
-          const int s = n / p.f;
-          const bf16* gsrc = p.gu + row * p.ldgu + s * 2 * p.f + (n - s * p.f);
-#pragma unroll
-          for (int vv = 0; vv < 4; ++vv) {
-            G[vv] = *reinterpret_cast<const uint4*>(gsrc + vv * 8);
-            U[vv] = *reinterpret_cast<const uint4*>(gsrc + p.f + vv * 8);
-          }
-        };
-        const uint4 z4 = make_uint4(0, 0, 0, 0);
-        if (!gu_ready) {
-#pragma unroll
-          for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
-          if (row_ok && ti.nb0 + grp * 32 < p.N) load_gu(grow, ti.nb0 + grp * 32, Gn, Un);
-        }
-        gu_ready = false;
-        const int sw = (lane >> 1) & 3;  // 64-byte swizzle of this lane's staging row
-#pragma unroll 1
-        for (int c = grp; c < BN / 32; c += NG) {
-          const int n = ti.nb0 + c * 32;  // column of dh within [0, S*f)
-          if (n >= p.N) break;
-          uint4 Gc[4], Uc[4], Hc[4];
-#pragma unroll
-          for (int vv = 0; vv < 4; ++vv) Hc[vv] = z4;
-          if (row_ok) {
-            const bf16* hsrc = p.h + grow * p.ldh + n;
-#pragma unroll
-            for (int vv = 0; vv < 4; ++vv) Hc[vv] = *reinterpret_cast<const uint4*>(hsrc + vv * 8);
-          }
-#pragma unroll
-          for (int vv = 0; vv < 4; ++vv) { Gc[vv] = Gn[vv]; Uc[vv] = Un[vv]; }
-          const bool more = c + NG < BN / 32 && n + 32 * NG < p.N;
-          if (more) {
-            if (row_ok) load_gu(grow, n + 32 * NG, Gn, Un);
-          } else if (t + tile_step<PAIR>() < total) {
-            // the warp's last chunk of this tile: fetch its first chunk of the next one
-            const Tile nt = tile_of<BN, PAIR>(p, ttab, Cfg<BN, EW, CW16>::TT_CAP, it + 1,
-                                              t + tile_step<PAIR>());
-            if (nt.rows - q * 32 > 0) {  // the next tile's epilogue runs for this warp
-#pragma unroll
-              for (int vv = 0; vv < 4; ++vv) { Gn[vv] = z4; Un[vv] = z4; }
-              if (r_loc < nt.rows && nt.nb0 + grp * 32 < p.N)
-                load_gu(static_cast<long long>(nt.m0) + r_loc, nt.nb0 + grp * 32, Gn, Un);
-              gu_ready = true;
-            }
-          }
-          float a[32];
-          ld_chunk(trow + c * 32, a);
-          const int s = n / p.f;
-          const int jj = n - s * p.f;
-          const int gcol = s * 2 * p.f + jj;
-          if (use_tma) stage_begin();
-          bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + gcol;
-#pragma unroll
-          for (int vv = 0; vv < 4; ++vv) {
-            const uint32_t Gw[4] = {Gc[vv].x, Gc[vv].y, Gc[vv].z, Gc[vv].w};
-            const uint32_t Uw[4] = {Uc[vv].x, Uc[vv].y, Uc[vv].z, Uc[vv].w};
-            const uint32_t Hw[4] = {Hc[vv].x, Hc[vv].y, Hc[vv].z, Hc[vv].w};
-            uint32_t pdg[4], pdu[4], phw[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              float dgv[2], duv[2], hwv[2];
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const float av = a[vv * 8 + 2 * e2 + hh];
-                const float gg = hh ? bf16_hi(Gw[e2]) : bf16_lo(Gw[e2]);
-                const float uu = hh ? bf16_hi(Uw[e2]) : bf16_lo(Uw[e2]);
-                const float hv = hh ? bf16_hi(Hw[e2]) : bf16_lo(Hw[e2]);
-                const float sg = sigmoidf_(gg);
-                const float dh = w * av;
-                dgv[hh] = dh * uu * sg * (1.0f + gg * (1.0f - sg));
-                duv[hh] = dh * gg * sg;
-                dot = fmaf(av, hv, dot);
-                hwv[hh] = w * hv;
-              }
-              pdg[e2] = pack_bf16(dgv[0], dgv[1]);
-              pdu[e2] = pack_bf16(duv[0], duv[1]);
-              phw[e2] = pack_bf16(hwv[0], hwv[1]);
-            }
-            const uint4 DG = make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]);
-            const uint4 DU = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
-            const uint4 HW = make_uint4(phw[0], phw[1], phw[2], phw[3]);
-            if (use_tma) {
-              const int off = lane * 64 + ((vv ^ sw) << 4);
-              *reinterpret_cast<uint4*>(stg + off) = DG;
-              *reinterpret_cast<uint4*>(stg + 2048 + off) = DU;
-              if (p.aux) *reinterpret_cast<uint4*>(stg + 4096 + off) = HW;
-            } else if (row_ok) {
-              store16(dgdst + vv * 8, DG);
-              store16(dgdst + p.f + vv * 8, DU);
-              if (p.aux) store16(p.aux + grow * p.ldaux + n + vv * 8, HW);
-            }
-          }
-          if (use_tma) {
-            stage_end();
-            if (lane == 0) {
-              tma_store_2d(sm.c0, stg_s, gcol, row0);
-              tma_store_2d(sm.c0, stg_s + 2048, gcol + p.f, row0);
-              if (p.aux) tma_store_2d(sm.c1, stg_s + 4096, n, row0);
-              bulk_commit();
-            }
-            pending = true;
-          }
-        }
-        if (row_ok && p.dw_part) p.dw_part[grow * p.dw_nparts + ti.n_blk * NG + grp] = dot;
-        }
       }
     }
     tc_fence_before();
@@ -1216,7 +1213,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   __syncwarp();
 }
 
-template <int BN, int EW, bool CW16, bool PAIR, int GW>
+template <int BN, int EW, bool CW16, bool PAIR, int GW, bool SBWD>
 __global__ void __launch_bounds__(64 + 32 * (EW + GW), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
@@ -1224,7 +1221,7 @@ __global__ void __launch_bounds__(64 + 32 * (EW + GW), 1)
                    const __grid_constant__ CUtensorMap mapC1,
                    const __grid_constant__ CUtensorMap mapA2,
                    const __grid_constant__ CUtensorMap mapB2, const Params p) {
-  using C = Cfg<BN, EW, CW16, PAIR>;
+  using C = Cfg<BN, EW, CW16, PAIR, SBWD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1236,6 +1233,8 @@ __global__ void __launch_bounds__(64 + 32 * (EW + GW), 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // SwiGLU-backward epilogue: three input-slot barriers per epilogue warp
+  uint64_t* lbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(full) + 256);
   int4* ttab = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(full) + MISC_BYTES);
   const int warp = threadIdx.x >> 5;
   if (p.sched != SCHED_DENSE && warp >= 2 && warp < 2 + EW) {
@@ -1244,7 +1243,7 @@ __global__ void __launch_bounds__(64 + 32 * (EW + GW), 1)
     const int mine = total > static_cast<int>(blockIdx.x)
                          ? (total - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
                          : 0;
-    const int n = mine < C::TT_CAP ? mine : C::TT_CAP;
+    const int n = mine < p.tt_cap ? mine : p.tt_cap;
     for (int i = threadIdx.x - 64; i < n; i += 32 * EW)
       ttab[i] = pack_tile<BN>(p, decode<BN>(p, blockIdx.x + i * gridDim.x));
   }
@@ -1261,6 +1260,8 @@ __global__ void __launch_bounds__(64 + 32 * (EW + GW), 1)
       mbar_init(&tempty[b], PAIR ? 2 * EW : 32 * EW);  // pairs: one arrival per warp of both CTAs
     }
     mbar_init(drain, 1);
+    if (SBWD)
+      for (int i = 0; i < 3 * EW; ++i) mbar_init(&lbar[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&mapA);
@@ -1283,22 +1284,27 @@ __global__ void __launch_bounds__(64 + 32 * (EW + GW), 1)
 
   if (warp == 0) {
     if (lane_id() == 0)
-      producer_loop<BN, EW, CW16, PAIR, GW>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty,
+      producer_loop<BN, EW, CW16, PAIR, GW, SBWD>(p, &mapA, &mapB, &mapA2, &mapB2, smem, full, empty,
                                             ttab, abort_flag);
   } else if (warp == 1) {
     if constexpr (!PAIR) {
-      mma_loop<BN, EW, CW16, GW>(p, smem, full, empty, tfull, tempty, drain, tmem_base, ttab,
+      mma_loop<BN, EW, CW16, GW, SBWD>(p, smem, full, empty, tfull, tempty, drain, tmem_base, ttab,
                                  abort_flag);
     } else {
       if (cluster_ctarank() == 0)  // the second CTA's MMA warp has nothing to do
-        mma_loop_pair<BN, EW, CW16>(p, smem, full, empty, tfull, tempty, drain, tmem_base,
+        mma_loop_pair<BN, EW, CW16, SBWD>(p, smem, full, empty, tfull, tempty, drain, tmem_base,
                                     abort_flag);
     }
   } else if (warp < 2 + EW) {
-    const StoreMaps sm{&mapC0, &mapC1, p.c0_rank3};
-    epilogue_loop<BN, EW, CW16, PAIR>(p, sm, staging, tfull, tempty, tmem_base, ttab, abort_flag);
+    const StoreMaps sm{&mapC0, &mapC1, p.c0_rank3, &mapA2, &mapB2};
+    if constexpr (SBWD)
+      epilogue_loop_sbwd<BN, PAIR>(p, sm, staging, lbar, tfull, tempty, tmem_base, ttab,
+                                   abort_flag);
+    else
+      epilogue_loop<BN, EW, CW16, PAIR>(p, sm, staging, tfull, tempty, tmem_base, ttab,
+                                        abort_flag);
   } else {
-    if constexpr (GW > 0 && !PAIR) gather_loop<BN, EW, CW16, GW>(p, smem, full, empty, ttab,
+    if constexpr (GW > 0 && !PAIR) gather_loop<BN, EW, CW16, GW, SBWD>(p, smem, full, empty, ttab,
                                                                  abort_flag);
   }
   tc_fence_before();
@@ -1388,11 +1394,13 @@ bool make_store_map(CUtensorMap* map, void* ptr, bool f32, bool rank3, long long
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int EW, bool CW16, bool PAIR, int GW = 0>
+template <int BN, int EW, bool CW16, bool PAIR, int GW = 0, bool SBWD = false>
 int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
-  using C = Cfg<BN, EW, CW16, PAIR>;
+  using C = Cfg<BN, EW, CW16, PAIR, SBWD>;
+  if (SBWD != (L.epi == EPI_SWIGLU_BWD)) return MOE_ERR_UNSUPPORTED;
   constexpr int THREADS = C::THREADS + 32 * GW;
   Params p{};
+  p.tt_cap = C::TT_CAP;
   p.pair = PAIR ? 1 : 0;
   p.sched = L.sched;
   p.M = L.M;
@@ -1534,6 +1542,9 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
     ok = make_store_map(&mapC0, L.C, false, false, L.ldc, rows_out, 1, L.ldc, 0);
     if (ok && L.aux)
       ok = make_store_map(&mapC1, L.aux, false, false, L.ldaux, rows_out, 1, L.ldaux, 0);
+    // the epilogue's inputs g|u and h, loaded in the same 32 x 32 blocks
+    if (ok) ok = make_store_map(&mapA2, L.gu, false, false, L.ldgu, rows_out, 1, L.ldgu, 0);
+    if (ok) ok = make_store_map(&mapB2, L.h, false, false, L.ldh, rows_out, 1, L.ldh, 0);
   }
   if (!ok) return MOE_ERR_ARG;
 
@@ -1541,7 +1552,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EW, CW16, PAIR, GW>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EW, CW16, PAIR, GW, SBWD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) {
@@ -1568,12 +1579,12 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     LaunchTimer lt(L.name, stream);
-    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EW, CW16, PAIR, GW>, mapA, mapB, mapC0, mapC1,
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EW, CW16, PAIR, GW, SBWD>, mapA, mapB, mapC0, mapC1,
                            mapA2, mapB2, p);
   } else {
     const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
     LaunchTimer lt(L.name, stream);
-    gemm_tc_kernel<BN, EW, CW16, PAIR, GW><<<grid, THREADS, C::SMEM_BYTES, stream>>>(
+    gemm_tc_kernel<BN, EW, CW16, PAIR, GW, SBWD><<<grid, THREADS, C::SMEM_BYTES, stream>>>(
         mapA, mapB, mapC0, mapC1, mapA2, mapB2, p);
     e = cudaSuccess;
   }
@@ -1625,42 +1636,44 @@ int gemm_epilogue_warps(const GemmLaunch& L) {
   // that one warp per TMEM lane quadrant cannot hide their latency: they get
   // 8 warps (and one pipeline stage less). Plain stores keep 4 warps and the
   // deeper pipeline.
-  return (L.epi == EPI_SWIGLU || L.epi == EPI_SWIGLU_BWD) ? 8 : 4;
+  return L.epi == EPI_SWIGLU ? 8 : 4;
 }
 
 int gemm_launch(const GemmLaunch& L, cudaStream_t stream) {
   const int ew = gemm_epilogue_warps(L);
   if (L.splitk > 1 && !(L.sched == SCHED_DENSE && L.epi == EPI_STORE && !L.accumulate))
     return MOE_ERR_UNSUPPORTED;
-  // The SwiGLU forward epilogue works on 16-column chunks (smaller staging, one
-  // more pipeline stage); its backward on 32-column chunks.
-  const bool cw16 = L.epi == EPI_SWIGLU;
+  // The SwiGLU forward epilogue (8 warps) works on 16-column chunks (smaller
+  // staging, one more pipeline stage); its backward runs epilogue_loop_sbwd.
   // CTA pairs (256-row tiles, cta_group::2 MMAs, half of B per CTA) for the dense
   // schedule with 256-wide tiles and at least two row blocks
   const bool gather = L.gather_a || L.gather_b;
   const bool pair = L.pair && L.BN == 256 && L.sched == SCHED_DENSE && L.K > 0 && L.M > BM &&
                     !gather;
   int st;
-  if (L.BN == 256 && pair)
+  if (L.epi == EPI_SWIGLU_BWD) {
+    // 4 epilogue warps with TMA-staged g, u, h (epilogue_loop_sbwd)
+    if (L.BN == 256 && pair) st = launch_bn<256, 4, false, true, 0, true>(L, stream);
+    else if (gather && L.BN == 256) st = launch_bn<256, 4, false, false, kGatherWarps, true>(L, stream);
+    else if (gather && L.BN == 128) st = launch_bn<128, 4, false, false, kGatherWarps, true>(L, stream);
+    else if (L.BN == 256) st = launch_bn<256, 4, false, false, 0, true>(L, stream);
+    else if (L.BN == 128) st = launch_bn<128, 4, false, false, 0, true>(L, stream);
+    else return MOE_ERR_UNSUPPORTED;
+  } else if (L.BN == 256 && pair)
     st = ew == 4 ? launch_bn<256, 4, false, true>(L, stream)
-                 : (cw16 ? launch_bn<256, 8, true, true>(L, stream)
-                         : launch_bn<256, 8, false, true>(L, stream));
+                 : launch_bn<256, 8, true, true>(L, stream);
   else if (gather && L.BN == 256)
     st = ew == 4 ? launch_bn<256, 4, false, false, kGatherWarps>(L, stream)
-                 : (cw16 ? launch_bn<256, 8, true, false, kGatherWarps>(L, stream)
-                         : launch_bn<256, 8, false, false, kGatherWarps>(L, stream));
+                 : launch_bn<256, 8, true, false, kGatherWarps>(L, stream);
   else if (gather && L.BN == 128)
     st = ew == 4 ? launch_bn<128, 4, false, false, kGatherWarps>(L, stream)
-                 : (cw16 ? launch_bn<128, 8, true, false, kGatherWarps>(L, stream)
-                         : launch_bn<128, 8, false, false, kGatherWarps>(L, stream));
+                 : launch_bn<128, 8, true, false, kGatherWarps>(L, stream);
   else if (L.BN == 256)
     st = ew == 4 ? launch_bn<256, 4, false, false>(L, stream)
-                 : (cw16 ? launch_bn<256, 8, true, false>(L, stream)
-                         : launch_bn<256, 8, false, false>(L, stream));
+                 : launch_bn<256, 8, true, false>(L, stream);
   else if (L.BN == 128)
     st = ew == 4 ? launch_bn<128, 4, false, false>(L, stream)
-                 : (cw16 ? launch_bn<128, 8, true, false>(L, stream)
-                         : launch_bn<128, 8, false, false>(L, stream));
+                 : launch_bn<128, 8, true, false>(L, stream);
   else
     return MOE_ERR_UNSUPPORTED;
   if (st != MOE_OK || L.splitk <= 1) return st;
