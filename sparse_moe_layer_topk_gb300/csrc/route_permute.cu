@@ -1,8 +1,9 @@
 // Routing, permute bookkeeping and row-movement kernels of libmoe (sm_103a).
 //
-//   topk_sigmoid_kernel   warp per token: top-k of (logit + bias) by warp
-//                         redux over 64-bit (value, ~id) keys, then sigmoid
-//                         and renormalisation.
+//   topk_sigmoid_kernel   warp per token: top-k of (logit + bias) among the
+//                         values that reach the k-th largest lane maximum, by
+//                         warp redux over 64-bit (value, ~id) keys, then
+//                         sigmoid and renormalisation.
 //   chunk_hist_kernel     per 256-token chunk (four threads per token): one bit
 //                         per (expert, token) in shared memory -> per-chunk
 //                         expert histogram.
@@ -32,13 +33,6 @@ namespace {
 constexpr int kChunk = 256;  // tokens per chunk of the histogram / maps kernels
 constexpr int kChunkThreads = 1024;  // 4 threads per token, each taking every 4th slot j
 
-// Order-preserving bits of a float; -0 and +0 are one value (they compare
-// equal, so a tie between them goes to the lower expert id like any other).
-__device__ __forceinline__ uint32_t order_key(float v) {
-  uint32_t u = __float_as_uint(v);
-  if (u == 0x80000000u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
@@ -46,13 +40,40 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 
 // Selection keys: (order-preserving bits of the value) << 32 | ~id, so a larger
 // key is a larger value or, for equal values, a lower expert id; 0 = no entry.
-__device__ __forceinline__ unsigned long long sel_key(float v, int e) {
-  return (static_cast<unsigned long long>(order_key(v)) << 32) |
+__device__ __forceinline__ unsigned long long sel_key(uint32_t value_key, int e) {
+  return (static_cast<unsigned long long>(value_key) << 32) |
          static_cast<unsigned long long>(~static_cast<uint32_t>(e));
+}
+
+// Order-preserving bits of a float, in two integer operations: negative values
+// have all bits flipped, non-negative ones the sign bit set. -0 and +0 are one
+// value (they compare equal, so a tie between them goes to the lower expert id
+// like any other): -0 is first made +0 by an IEEE add of +0, on the
+// floating-point pipe.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+  return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+}
+
+// Warp-wide maximum of 64-bit keys, as two 32-bit reductions: the high words,
+// then the low words of the lanes holding the maximal high word.
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long x) {
+  const uint32_t mh = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(x >> 32));
+  const uint32_t ml = __reduce_max_sync(
+      0xFFFFFFFFu, static_cast<uint32_t>(x >> 32) == mh ? static_cast<uint32_t>(x) : 0u);
+  return (static_cast<unsigned long long>(mh) << 32) | ml;
 }
 
 // NPL keys per lane. VEC (E a multiple of 128): lane holds experts
 // 128 i + 4 lane + j, read as float4; otherwise experts lane + 32 i.
+//
+// Fast path: every one of the k largest values is at least tau, the k-th
+// largest of the 32 lanes' maxima (those k maxima are k values >= tau). The
+// values >= tau (typically a few dozen of E) are compacted into shared memory,
+// at most two per lane, and k rounds of a warp-wide maximum pick them in order.
+// When more than 64 values reach tau (many equal values, or k close to 32),
+// the selection falls back to k rounds over all of the lanes' keys, each lane
+// tracking its largest and second largest key.
 template <int NPL, bool VEC>
 __global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __restrict__ L,
                                                               const float* __restrict__ bias,
@@ -61,11 +82,15 @@ __global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __res
                                                               float* __restrict__ w_out,
                                                               float* __restrict__ s_out,
                                                               int* err_flag) {
+  __shared__ unsigned long long cand_s[8][64];  // 256 threads: 8 warps, one token each
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
   if (t >= T) return;
   const float* row = L + static_cast<size_t>(t) * E;
-  unsigned long long key[NPL];
+  auto expert_of = [&](int i) { return VEC ? 128 * (i >> 2) + 4 * lane + (i & 3) : lane + 32 * i; };
+  auto valid_at = [&](int i) { return VEC ? 128 * (i >> 2) < E : lane + 32 * i < E; };
+  uint32_t kv[NPL];  // order keys of logit + bias; 0 where this lane holds no expert
   bool bad = false;
   if (VEC) {
     float4 lv[NPL / 4 > 0 ? NPL / 4 : 1];
@@ -82,9 +107,9 @@ __global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __res
         if (128 * i < E) {
           const float v = vv[j] + (bias ? __ldg(bias + e) : 0.0f);
           bad |= !isfinite(v);
-          key[4 * i + j] = sel_key(v, e);
+          kv[4 * i + j] = order_key(v);
         } else {
-          key[4 * i + j] = 0ull;
+          kv[4 * i + j] = 0u;
         }
       }
     }
@@ -95,40 +120,94 @@ __global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __res
       if (e < E) {
         const float v = __ldg(row + e) + (bias ? __ldg(bias + e) : 0.0f);
         bad |= !isfinite(v);
-        key[i] = sel_key(v, e);
+        kv[i] = order_key(v);
       } else {
-        key[i] = 0ull;
+        kv[i] = 0u;
       }
     }
   }
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_flag(err_flag, MOE_FLAG_NONFINITE);
-  // this lane's largest and second largest key
-  unsigned long long b1 = 0ull, b2 = 0ull;
+  // tau: the k-th largest lane maximum (bitonic sort of the 32 maxima, descending)
+  uint32_t mx = 0u;
 #pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    if (key[i] > b1) { b2 = b1; b1 = key[i]; } else if (key[i] > b2) { b2 = key[i]; }
+  for (int i = 0; i < NPL; ++i) mx = max(mx, kv[i]);
+  uint32_t srt = mx;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, srt, stride);
+      const bool take_max = ((lane & size) == 0) == ((lane & stride) == 0);
+      srt = take_max ? max(srt, o) : min(srt, o);
+    }
   }
-  bool has2 = true;
-  unsigned long long mine = 0ull;  // the j-th selection, kept by lane j
-  for (int j = 0; j < k; ++j) {
-    // warp-wide maximum key: high words first, then the low words of the lanes holding it
-    const uint32_t mh = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(b1 >> 32));
-    const uint32_t ml = __reduce_max_sync(
-        0xFFFFFFFFu, static_cast<uint32_t>(b1 >> 32) == mh ? static_cast<uint32_t>(b1) : 0u);
-    const unsigned long long m = (static_cast<unsigned long long>(mh) << 32) | ml;
-    if (lane == j) mine = m;
-    if (b1 == m) {
-      // The winner's keys at or above m are all taken (a lane always gives up its
-      // largest remaining key), so its next key is its second largest, or the
-      // largest key below m once the second has been used as well.
-      if (has2) {
-        b1 = b2;
-        has2 = false;
-      } else {
-        b1 = 0ull;
+  const uint32_t tau = __shfl_sync(0xFFFFFFFFu, srt, k - 1);
+  uint32_t cmask = 0u;  // bit i: kv[i] reaches tau
 #pragma unroll
-        for (int i = 0; i < NPL; ++i)
-          if (key[i] < m && key[i] > b1) b1 = key[i];
+  for (int i = 0; i < NPL; ++i) cmask |= (valid_at(i) && kv[i] >= tau) ? (1u << i) : 0u;
+  const int cnt = __popc(cmask);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  unsigned long long mine = 0ull;  // the j-th selection, kept by lane j
+  if (total <= 64) {
+    unsigned long long* cs = cand_s[wib];
+    int pos = incl - cnt;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (cmask & (1u << i)) cs[pos++] = sel_key(kv[i], expert_of(i));
+    for (int q = total + lane; q < 64; q += 32) cs[q] = 0ull;
+    __syncwarp();
+    unsigned long long c0 = cs[lane], c1 = cs[lane + 32];
+    if (c1 > c0) { const unsigned long long x = c0; c0 = c1; c1 = x; }
+    for (int j = 0; j < k; ++j) {
+      // the value maximum first; the id reduction only when values tie exactly
+      const uint32_t hi = static_cast<uint32_t>(c0 >> 32);
+      const uint32_t mh = __reduce_max_sync(0xFFFFFFFFu, hi);
+      const unsigned tied = __ballot_sync(0xFFFFFFFFu, hi == mh);
+      unsigned long long m;
+      if (__popc(tied) == 1) {
+        m = __shfl_sync(0xFFFFFFFFu, c0, __ffs(tied) - 1);
+      } else {
+        const uint32_t ml =
+            __reduce_max_sync(0xFFFFFFFFu, hi == mh ? static_cast<uint32_t>(c0) : 0u);
+        m = (static_cast<unsigned long long>(mh) << 32) | ml;
+      }
+      if (lane == j) mine = m;
+      if (c0 == m) { c0 = c1; c1 = 0ull; }
+    }
+  } else {
+    unsigned long long key[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      key[i] = valid_at(i) ? sel_key(kv[i], expert_of(i)) : 0ull;
+    // this lane's largest and second largest key
+    unsigned long long b1 = 0ull, b2 = 0ull;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      if (key[i] > b1) { b2 = b1; b1 = key[i]; } else if (key[i] > b2) { b2 = key[i]; }
+    }
+    bool has2 = true;
+    for (int j = 0; j < k; ++j) {
+      const unsigned long long m = warp_max_key(b1);
+      if (lane == j) mine = m;
+      if (b1 == m) {
+        // The winner's keys at or above m are all taken (a lane always gives up its
+        // largest remaining key), so its next key is its second largest, or the
+        // largest key below m once the second has been used as well.
+        if (has2) {
+          b1 = b2;
+          has2 = false;
+        } else {
+          b1 = 0ull;
+#pragma unroll
+          for (int i = 0; i < NPL; ++i)
+            if (key[i] < m && key[i] > b1) b1 = key[i];
+        }
       }
     }
   }
