@@ -48,6 +48,9 @@ struct GemmLaunch {
   const int* expert_order = nullptr;  // grouped-M: groups walked in this order (tile_sched
                                       // is then the scan in that order); nullptr = natural
   int R_cap = 0;                    // row capacity (SCHED_GROUPED_M grid bound)
+  // Grouped-M tile shape per tile: a tile of at most 64 rows (an expert's last
+  // rows, or a small expert) runs M = 64 MMAs, half the tensor work of M = 128.
+  int m64 = 1;
   // operands: A is [M][K] (a_mn = 0) or [K][M] (a_mn = 1);
   //           B is [N][K] (b_mn = 0) or [K][N] (b_mn = 1), optionally batched.
   MatView A, B;

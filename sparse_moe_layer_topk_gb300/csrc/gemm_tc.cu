@@ -116,6 +116,7 @@ struct Params {
   long long gld;
   int gwidth;
   int tt_cap;  // tiles of a CTA held in its shared-memory table (the rest are decoded inline)
+  int m64;     // grouped-M: tiles of at most 64 rows run M = 64 MMAs (see quad_rows)
   int pair;  // 1: CTA pairs (cluster of 2) own 256-row tiles (dense schedule)
   int mt2;   // pair rows of tiles: ceil(mt / 2)
 };
@@ -131,6 +132,15 @@ struct Tile {
   int krows;   // valid K rows (grouped-K), else K
   int nk;      // number of 64-wide K blocks
 };
+
+// Rows of the accumulator in each tensor-memory lane quadrant. An M = 128 MMA
+// puts row r in lane r (32 rows per quadrant); an M = 64 MMA (grouped-M tiles
+// of at most 64 rows when p.m64) puts rows 16q .. 16q+15 in lanes 32q ..
+// 32q+15 of quadrant q. The epilogue warp of quadrant q reads its 32 lanes and
+// uses the first quad_rows of them.
+__device__ __forceinline__ int quad_rows(const Params& p, int rows) {
+  return (p.m64 && p.sched == SCHED_GROUPED_M && rows <= 64) ? 16 : 32;
+}
 
 __device__ __forceinline__ int total_tiles(const Params& p) {
   if (p.sched == SCHED_GROUPED_M) return __ldg(p.tile_sched + p.G) * p.nt;
@@ -542,7 +552,8 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
                          const int4* ttab, volatile int* abort_flag) {
   using C = Cfg<BN, EW, CW16, false, SBWD>;
   const uint32_t lane = lane_id();
-  const uint32_t idesc = make_idesc_bf16(BM, BN, p.a_mn, p.b_mn);
+  const uint32_t idesc128 = make_idesc_bf16(BM, BN, p.a_mn, p.b_mn);
+  const uint32_t idesc64 = make_idesc_bf16(64, BN, p.a_mn, p.b_mn);
   const uint32_t a_lbo = p.a_mn ? CHUNK_BYTES : 16, b_lbo = p.b_mn ? CHUNK_BYTES : 16;
   const uint32_t a_kstep = p.a_mn ? 2048 : 32, b_kstep = p.b_mn ? 2048 : 32;
   int stage = 0;
@@ -553,6 +564,7 @@ __device__ void mma_loop(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   bool ok = true;
   for (int t = tile_begin<false>(); t < total && ok; t += tile_step<false>(), ++it) {
     const Tile ti = tile_of<BN>(p, ttab, it, t);
+    const uint32_t idesc = quad_rows(p, ti.rows) == 16 ? idesc64 : idesc128;
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
     if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
@@ -857,7 +869,8 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
         a_ti = tile_of<BN, PAIR>(p, ttab, a_it, a_t);
         a_have = true;
       }
-      if (a_ti.rows - q * 32 > 0 && a_c < NCH && a_ti.nb0 + 32 * a_c < p.N) return true;
+      if (a_ti.rows - q * quad_rows(p, a_ti.rows) > 0 && a_c < NCH && a_ti.nb0 + 32 * a_c < p.N)
+        return true;
       a_c = 0;
       a_t += tile_step<PAIR>();
       ++a_it;
@@ -870,7 +883,7 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
     const int n = a_ti.nb0 + 32 * a_c;
     const int sx = n / p.f;
     const int gcol = sx * 2 * p.f + (n - sx * p.f);
-    const int row0 = a_ti.m0 + q * 32;
+    const int row0 = a_ti.m0 + q * quad_rows(p, a_ti.rows);
     const int slot = static_cast<int>(issued % 3);
     if (lane == 0) {
       const uint32_t d = smem_u32(slots + slot * SLOT);
@@ -896,15 +909,16 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
       break;
     }
     tc_fence_after();
-    const int blk_rows = ti.rows - q * 32;
-    const int r_loc = q * 32 + static_cast<int>(lane);
-    const bool row_ok = r_loc < ti.rows;
+    const int qr = quad_rows(p, ti.rows);
+    const int blk_rows = ti.rows - q * qr;
+    const int r_loc = q * qr + static_cast<int>(lane);
+    const bool row_ok = static_cast<int>(lane) < qr && r_loc < ti.rows;
     const long long grow = static_cast<long long>(ti.m0) + r_loc;
-    const int row0 = ti.m0 + q * 32;
+    const int row0 = ti.m0 + q * qr;
     const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(buf * BN);
-    // TMA clips outside the tensor; inside it (grouped-M) only full blocks may use it
-    const bool use_tma = blk_rows >= 32 || p.sched != SCHED_GROUPED_M;
+    // TMA clips outside the tensor; inside it (grouped-M) only full 32-row blocks may use it
+    const bool use_tma = qr == 32 && (blk_rows >= 32 || p.sched != SCHED_GROUPED_M);
     if (blk_rows > 0) {
       const float w = (row_ok && p.row_w) ? __ldg(p.row_w + grow) : 1.0f;
       float dot = 0.0f;
@@ -996,7 +1010,6 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   const int q = warp & 3;  // tensor-memory lane quadrant this warp may read
   const int grp = (warp - 2) / 4;
   const uint32_t lane = lane_id();
-  const int r_loc = q * 32 + static_cast<int>(lane);
   uint8_t* const stg0 = staging + (warp - 2) * Cfg<BN, EW, CW16>::STG;
   // slot of one chunk (1 KB multiples keep every swizzle span aligned)
   int slot_bytes;
@@ -1034,15 +1047,17 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
       break;
     }
     tc_fence_after();
-    const int blk_rows = ti.rows - q * 32;  // valid rows of this warp's 32-row block
-    const bool row_ok = r_loc < ti.rows;
+    const int qr = quad_rows(p, ti.rows);  // accumulator rows in this warp's quadrant
+    const int r_loc = q * qr + static_cast<int>(lane);
+    const int blk_rows = ti.rows - q * qr;  // valid rows of this warp's block
+    const bool row_ok = static_cast<int>(lane) < qr && r_loc < ti.rows;
     const long long grow = static_cast<long long>(ti.m0) + r_loc;
-    const int row0 = ti.m0 + q * 32;
+    const int row0 = ti.m0 + q * qr;
     const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(buf * BN);
     const bool has_acc = ti.nk > 0;
-    // TMA clips outside the tensor; inside it (grouped-M) only full blocks may use it.
-    const bool use_tma = blk_rows >= 32 || p.sched != SCHED_GROUPED_M;
+    // TMA clips outside the tensor; inside it (grouped-M) only full 32-row blocks may use it.
+    const bool use_tma = qr == 32 && (blk_rows >= 32 || p.sched != SCHED_GROUPED_M);
 
     if (blk_rows > 0) {
       if (p.epi == EPI_STORE) {
@@ -1401,6 +1416,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   constexpr int THREADS = C::THREADS + 32 * GW;
   Params p{};
   p.tt_cap = C::TT_CAP;
+  p.m64 = (L.m64 && L.sched == SCHED_GROUPED_M) ? 1 : 0;
   p.pair = PAIR ? 1 : 0;
   p.sched = L.sched;
   p.M = L.M;
