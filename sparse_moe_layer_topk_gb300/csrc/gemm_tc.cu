@@ -47,7 +47,8 @@ constexpr int kGatherWarps = 2;
 // PAIR: the CTA is one of a pair computing 256-row tiles with cta_group::2 MMAs
 // (each CTA holds its 128 rows of A and half of B's columns).
 // SBWD: the SwiGLU-backward epilogue with TMA-staged inputs (4 warps, each
-// with three 6 KB slots for a chunk's g, u and h blocks).
+// with a ring of SLOTS 6 KB slots for a chunk's g, u and h blocks: four where
+// the stages leave room (32 KB stages), else three).
 template <int BN, int EW, bool CW16 = false, bool PAIR = false, bool SBWD = false>
 struct Cfg {
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
@@ -64,7 +65,8 @@ struct Cfg {
   // the next chunks are staged: one fp32 / three bf16 slots with 4 epilogue
   // warps (a whole tile table of a ragged-K weight gradient measured faster
   // than a second fp32 slot), one SwiGLU chunk with 8.
-  static constexpr int STG = SBWD ? 3 * 6144 : (CW16 ? 3072 : (EW == 8 ? 6144 : 7168));
+  static constexpr int SLOTS = (PAIR || BN == 128) ? 4 : 3;
+  static constexpr int STG = SBWD ? SLOTS * 6144 : (CW16 ? 3072 : (EW == 8 ? 6144 : 7168));
   // The rest of the 227 KB (after 1 KB alignment slack and the barriers) holds
   // the CTA's table of decoded grouped tiles, 16 bytes per tile.
   static constexpr int SMEM_LIMIT = 232448;
@@ -834,9 +836,9 @@ __device__ __forceinline__ void swiglu_bwd8(const float* a, uint4 G, uint4 U, ui
 
 // SwiGLU-backward epilogue with TMA-staged inputs. Each of the 4 epilogue
 // warps owns the 32 accumulator rows of its tensor-memory lane quadrant and a
-// ring of three 6 KB slots in shared memory; a slot holds the g, u and h blocks
+// ring of 6 KB slots in shared memory (Cfg::SLOTS); a slot holds the g, u and h blocks
 // (32 rows x 32 columns, bf16, 64-byte rows with 64-byte swizzle) of one
-// 32-column chunk. Lane 0 loads them by TMA two chunks ahead of the chunk being
+// 32-column chunk. Lane 0 loads them by TMA SLOTS - 1 chunks ahead of the chunk being
 // computed (across tile boundaries too). The chunk's dg, du and w*h overwrite g,
 // u and h in place and leave by TMA store from the same slot. (Loading the
 // inputs lane by lane instead makes every load instruction touch 32 rows, so
@@ -847,13 +849,14 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
                                    uint32_t tmem_base, const int4* ttab, volatile int* abort_flag) {
   using C = Cfg<BN, 4, false, PAIR, true>;
   constexpr int SLOT = 6144;
+  constexpr int NS = C::SLOTS;  // ring depth; inputs are requested NS - 1 chunks ahead
   constexpr int NCH = BN / 32;
   const int warp = static_cast<int>(threadIdx.x) >> 5;
   const int q = warp & 3;
   const int ew = warp - 2;
   const uint32_t lane = lane_id();
   uint8_t* const slots = staging + ew * C::STG;
-  uint64_t* const lb = lbar + 3 * ew;
+  uint64_t* const lb = lbar + NS * ew;
   const int total = total_tiles(p);
   const int sw = (static_cast<int>(lane) >> 1) & 3;  // 64-byte swizzle of this lane's row
 
@@ -884,7 +887,7 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
     const int sx = n / p.f;
     const int gcol = sx * 2 * p.f + (n - sx * p.f);
     const int row0 = a_ti.m0 + q * quad_rows(p, a_ti.rows);
-    const int slot = static_cast<int>(issued % 3);
+    const int slot = static_cast<int>(issued % NS);
     if (lane == 0) {
       const uint32_t d = smem_u32(slots + slot * SLOT);
       mbar_arrive_expect_tx(&lb[slot], SLOT);
@@ -895,7 +898,7 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
     ++issued;
     ++a_c;
   };
-  for (int i = 0; i < 2 && a_seek(); ++i) issue();
+  for (int i = 0; i < NS - 1 && a_seek(); ++i) issue();
 
   long long done = 0;  // jobs computed
   bool ok = true;
@@ -925,10 +928,10 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
       for (int c = 0; c < NCH; ++c) {
         const int n = ti.nb0 + c * 32;
         if (n >= p.N) break;
-        const int slot = static_cast<int>(done % 3);
+        const int slot = static_cast<int>(done % NS);
         int okw = 1;
         if (lane == 0)
-          okw = mbar_wait(&lb[slot], static_cast<uint32_t>((done / 3) & 1), abort_flag) ? 1 : 0;
+          okw = mbar_wait(&lb[slot], static_cast<uint32_t>((done / NS) & 1), abort_flag) ? 1 : 0;
         okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
         if (!okw) {
           if (lane == 0) raise_abort(abort_flag, p.err_flag);
@@ -995,7 +998,7 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
   if (lane == 0) {
     volatile int never = 0;
     for (long long j = done; j < issued; ++j)
-      mbar_wait(&lb[j % 3], static_cast<uint32_t>((j / 3) & 1), &never);
+      mbar_wait(&lb[j % NS], static_cast<uint32_t>((j / NS) & 1), &never);
     bulk_wait_all();
   }
   __syncwarp();
@@ -1276,7 +1279,7 @@ __global__ void __launch_bounds__(64 + 32 * (EW + GW), 1)
     }
     mbar_init(drain, 1);
     if (SBWD)
-      for (int i = 0; i < 3 * EW; ++i) mbar_init(&lbar[i], 1);
+      for (int i = 0; i < C::SLOTS * EW; ++i) mbar_init(&lbar[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&mapA);
