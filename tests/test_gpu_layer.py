@@ -178,22 +178,29 @@ def test_layer_full_size_forward(cfg_id):
         assert (counts <= 2).sum() >= 150 and (counts == 0).sum() > 0
 
 
-def test_layer_T2048_E896_every_output_and_gradient():
+@pytest.mark.parametrize("cfg_id", [1, 2])
+def test_layer_T2048_E896_every_output_and_gradient(cfg_id):
     """The layer at the 896-expert shapes (d=4096, l=1024, E=896 top-16, S=2,
-    f=512) with T=2048 tokens: every output and every gradient (out, dx, d_w,
-    dWr, dW_dn, dW13, dW2, dW13_sh, dW2_sh, dW_up) against the full fp64 oracle
-    on the same inputs. This runs the router's 896 columns (three 256-wide
-    tiles and a 128-wide tail) in the logits and in dWr, and the K-split
-    shared-expert weight gradients (2 slices at K = 2048). Routing is staged:
-    the GPU's ids are checked bit for bit against the oracle's selection on the
-    GPU's fp32 logits, and the oracle then runs on those ids, so no token is
-    excluded from any comparison."""
-    inp = I.make_layer_inputs(1, T=2048)
+    f=512) with T=2048 tokens, uniform (1) and Zipf-skewed (2) routing: every
+    output and every gradient (out, dx, d_w, dWr, dW_dn, dW13, dW2, dW13_sh,
+    dW2_sh, dW_up) against the full fp64 oracle on the same inputs. This runs
+    the router's 896 columns (three 256-wide tiles and a 128-wide tail) in the
+    logits and in dWr, the K-split shared-expert weight gradients (2 slices at
+    K = 2048), and, skewed, empty experts (exact-zero gradients) next to
+    experts of many row tiles. Routing is staged: the GPU's ids are checked bit
+    for bit against the oracle's selection on the values the GPU decided on,
+    and the oracle then runs on those ids, so no token is excluded from any
+    comparison."""
+    inp = I.make_layer_inputs(cfg_id, T=2048)
     cfg = inp["cfg"]
     layer = _run(inp)
     L = O.router_logits(inp["x"], inp["Wr"], inp["bias"])
-    gi, _ = _check_routing_staged(layer, cfg.k, L, 4)
-    _check_maps(layer, gi, cfg.E)
+    gi, _ = _check_routing_staged(layer, cfg.k, L, 4, inp["bias"])
+    counts = _check_maps(layer, gi, cfg.E)
+    if cfg.skew:
+        empty = np.where(counts == 0)[0]
+        assert empty.size > 0 and counts.max() > 4 * 128
+        assert not layer.grads["W13"][empty].any() and not layer.grads["W2"][empty].any()
     fwd = O.layer_forward(inp, idx=gi)
     check_close("w", f64(layer.topk_w), fwd["w"], max_abs=1e-5, rel_fro=1e-5)
     for name in ("z", "y_lat", "out"):
