@@ -500,7 +500,7 @@ __device__ void gather_loop(const Params& p, uint8_t* smem, uint64_t* full, uint
   bool ok = true;
   while (t < total && ok) {
     const int tn = t + tile_step<false>();
-    Tile nt;
+    Tile nt = ti;  // (unused when this is the last tile)
     if (tn < total) {
       nt = tile_of<BN>(p, ttab, it + 1, tn);
       if (gm) rows_m(nt, nidx_m);

@@ -75,7 +75,7 @@ __device__ __forceinline__ unsigned long long warp_max_key(unsigned long long x)
 // the selection falls back to k rounds over all of the lanes' keys, each lane
 // tracking its largest and second largest key.
 template <int NPL, bool VEC>
-__global__ void __launch_bounds__(256, 2) topk_sigmoid_kernel(const float* __restrict__ L,
+__global__ void __launch_bounds__(256, 4) topk_sigmoid_kernel(const float* __restrict__ L,
                                                               const float* __restrict__ bias,
                                                               int T, int E, int k,
                                                               int* __restrict__ idx,
