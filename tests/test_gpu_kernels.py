@@ -375,9 +375,10 @@ def test_host_argument_errors_do_not_launch():
 @pytest.mark.parametrize("T,E,k,l,f,skew", [(300, 37, 4, 128, 64, 1.5), (2048, 64, 8, 1024, 512, 0.0),
                                              (1, 16, 4, 256, 128, 0.0)])
 def test_gather_fused_grouped_gemms_equal_explicit_permute(T, E, k, l, f, skew):
-    """moe_grouped_swiglu[_bwd]_gather (rows gathered by TMA inside the GEMMs)
-    produce bit-identical results to the explicit permute followed by the
-    plain grouped calls: the same bytes land in the same shared-memory tiles."""
+    """moe_grouped_swiglu[_bwd]_gather (rows copied into the GEMMs' shared-memory
+    stages by the gather warps) produce bit-identical results to the explicit
+    permute followed by the plain grouped calls: the same bytes land in the same
+    shared-memory tiles."""
     idx = I.make_topk_ids(50 + T, T, E, k, skew=skew)
     z = _bf16(51, T, l)
     dy_lat = _bf16(52, T, l)
