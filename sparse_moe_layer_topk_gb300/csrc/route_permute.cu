@@ -65,16 +65,18 @@ __device__ __forceinline__ unsigned long long warp_max_key(unsigned long long x)
 }
 
 // NPL keys per lane. VEC (E a multiple of 128): lane holds experts
-// 128 i + 4 lane + j, read as float4; otherwise experts lane + 32 i.
+// 128 i + 4 lane + j, read as float4; otherwise experts lane + 32 i. FULL:
+// E = 32 NPL, every lane holds NPL experts.
 //
 // Fast path: every one of the k largest values is at least tau, the k-th
 // largest of the 32 lanes' maxima (those k maxima are k values >= tau). The
-// values >= tau (typically a few dozen of E) are compacted into shared memory,
-// at most two per lane, and k rounds of a warp-wide maximum pick them in order.
-// When more than 64 values reach tau (many equal values, or k close to 32),
-// the selection falls back to k rounds over all of the lanes' keys, each lane
-// tracking its largest and second largest key.
-template <int NPL, bool VEC>
+// values >= tau (typically about twenty of 896) are compacted into shared
+// memory; up to 32 of them are put in order by one bitonic sort across the
+// warp (lane j then holds the j-th largest), up to 64 by k rounds of a
+// warp-wide maximum. When more than 64 values reach tau (many equal values, or
+// k close to 32), the selection falls back to k rounds over all of the lanes'
+// keys, each lane tracking its largest and second largest key.
+template <int NPL, bool VEC, bool FULL>
 __global__ void __launch_bounds__(256, 4) topk_sigmoid_kernel(const float* __restrict__ L,
                                                               const float* __restrict__ bias,
                                                               int T, int E, int k,
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(256, 4) topk_sigmoid_kernel(const float* __res
         const int e = 128 * i + 4 * lane + j;
         if (128 * i < E) {
           const float v = vv[j] + (bias ? __ldg(bias + e) : 0.0f);
-          bad |= !isfinite(v);
+          if (!FULL) bad |= !isfinite(v);
           kv[4 * i + j] = order_key(v);
         } else {
           kv[4 * i + j] = 0u;
@@ -119,18 +121,26 @@ __global__ void __launch_bounds__(256, 4) topk_sigmoid_kernel(const float* __res
       const int e = lane + 32 * i;
       if (e < E) {
         const float v = __ldg(row + e) + (bias ? __ldg(bias + e) : 0.0f);
-        bad |= !isfinite(v);
+        if (!FULL) bad |= !isfinite(v);
         kv[i] = order_key(v);
       } else {
         kv[i] = 0u;
       }
     }
   }
-  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_flag(err_flag, MOE_FLAG_NONFINITE);
   // tau: the k-th largest lane maximum (bitonic sort of the 32 maxima, descending)
   uint32_t mx = 0u;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) mx = max(mx, kv[i]);
+  if (FULL) {
+    // The order keys of the finite values lie strictly between those of -inf
+    // (0x007FFFFF) and +inf (0xFF800000); NaNs fall outside them too.
+    uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) mn = min(mn, kv[i]);
+    bad = mx >= 0xFF800000u || mn <= 0x007FFFFFu;
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_flag(err_flag, MOE_FLAG_NONFINITE);
   uint32_t srt = mx;
 #pragma unroll
   for (int size = 2; size <= 32; size <<= 1) {
@@ -144,7 +154,7 @@ __global__ void __launch_bounds__(256, 4) topk_sigmoid_kernel(const float* __res
   const uint32_t tau = __shfl_sync(0xFFFFFFFFu, srt, k - 1);
   uint32_t cmask = 0u;  // bit i: kv[i] reaches tau
 #pragma unroll
-  for (int i = 0; i < NPL; ++i) cmask |= (valid_at(i) && kv[i] >= tau) ? (1u << i) : 0u;
+  for (int i = 0; i < NPL; ++i) cmask |= ((FULL || valid_at(i)) && kv[i] >= tau) ? (1u << i) : 0u;
   const int cnt = __popc(cmask);
   int incl = cnt;
 #pragma unroll
@@ -160,6 +170,23 @@ __global__ void __launch_bounds__(256, 4) topk_sigmoid_kernel(const float* __res
 #pragma unroll
     for (int i = 0; i < NPL; ++i)
       if (cmask & (1u << i)) cs[pos++] = sel_key(kv[i], expert_of(i));
+    __syncwarp();
+  }
+  if (total <= 32) {
+    // one candidate per lane (0 past them), sorted descending across the warp
+    unsigned long long c = lane < total ? cand_s[wib][lane] : 0ull;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, c, stride);
+        const bool take_max = ((lane & size) == 0) == ((lane & stride) == 0);
+        c = take_max ? (o > c ? o : c) : (o < c ? o : c);
+      }
+    }
+    mine = c;
+  } else if (total <= 64) {
+    unsigned long long* cs = cand_s[wib];
     for (int q = total + lane; q < 64; q += 32) cs[q] = 0ull;
     __syncwarp();
     unsigned long long c0 = cs[lane], c1 = cs[lane + 32];
@@ -613,8 +640,11 @@ cudaError_t launch_topk(const float* L, const float* bias, int T, int E, int k, 
   const int npl = (E + 31) / 32;
   LaunchTimer lt("topk_sigmoid", st);
   const bool vec = (E % 128) == 0 && (reinterpret_cast<uintptr_t>(L) & 15u) == 0;
-#define MOE_TOPK(N, V) topk_sigmoid_kernel<N, V><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag)
-  if (vec) {
+#define MOE_TOPK(N, V) topk_sigmoid_kernel<N, V, false><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s, err_flag)
+  if (vec && E == 32 * 28) {
+    topk_sigmoid_kernel<28, true, true><<<grid, 256, 0, st>>>(L, bias, T, E, k, idx, w, s,
+                                                             err_flag);
+  } else if (vec) {
     if (npl <= 4) MOE_TOPK(4, true);
     else if (npl <= 8) MOE_TOPK(8, true);
     else if (npl <= 16) MOE_TOPK(16, true);
