@@ -28,6 +28,10 @@ Sources (the pages give the structure, not the formulas):
   [AUX]   "大模型落地昇腾:从适配挑战到高效训练实践" page, section "三、通信侧":
           an auxiliary load-balance loss that constrains the entropy of the
           routing distribution.
+  [SWAP]  "昇腾实现Kimi K3.1 Pro模型LoRA训练适配" page, section "Swap Core:算子级
+          精准缓存与异步 Offload 协同,训练性能提升 15%": the outputs of selected
+          MatMul/GMM operators are cached for the backward, optionally compressed
+          by FP8 activation quantization and dequantization.
 Readings where the pages are silent (router = sigmoid(x@Wr) with renormalised
 top-k weights, lower expert id wins ties, tokens of an expert in ascending
 token order, shared experts in latent space with weight 1, routing weight
@@ -48,7 +52,8 @@ __all__ = [
     "grouped_swiglu", "combine", "layer_forward", "layer_backward",
     "ep_rank_forward", "m_tiles_schedule", "router_backward", "swiglu_expert_backward",
     "aux_balance_loss", "aux_balance_loss_backward", "replica_plan", "bucket_order",
-    "expert_bucket_class",
+    "expert_bucket_class", "e4m3_round", "fp8_block_scale", "fp8_block_quantize",
+    "fp8_block_dequantize", "FP8_BLOCK",
 ]
 
 
@@ -195,6 +200,63 @@ def combine(y_perm, slot_of, y_shared=None):
 
 
 # --------------------------------------------------------------------------
+# FP8 cache of the GMM outputs  [SWAP]
+# --------------------------------------------------------------------------
+# Reading (the page names FP8 activation quantization, not its format): OCP
+# FP8 E4M3 (4 exponent bits with bias 7, 3 mantissa bits, subnormals, largest
+# finite value 448, no infinities), round to nearest with ties to the even
+# mantissa, saturating at +-448; one power-of-two scale per row and block of
+# FP8_BLOCK consecutive columns, the smallest that brings the block's largest
+# magnitude to at most 448 (power of two: scaling is exact, so the rounding
+# decisions depend on the values alone).
+
+FP8_BLOCK = 128
+E4M3_MAX = 448.0
+
+
+def e4m3_round(y) -> np.ndarray:
+    """The E4M3 value nearest to y (ties to even mantissa), clamped to +-448."""
+    y = np.asarray(y, dtype=np.float64)
+    a = np.abs(y)
+    _, ex = np.frexp(a)                       # a = m 2^ex, 0.5 <= m < 1
+    E = np.maximum(ex - 1, -6)                # binade exponent; subnormals share 2^-6's
+    spacing = np.ldexp(1.0, E - 3)            # 3 mantissa bits
+    q = np.minimum(np.round(a / spacing) * spacing, E4M3_MAX)   # np.round: half to even
+    return np.where(y < 0, -q, q)
+
+
+def fp8_block_scale(amax: float) -> float:
+    """Smallest power of two s with amax <= 448 s (1 for amax < 2^-100)."""
+    amax = float(amax)
+    if not amax >= 2.0 ** -100:
+        return 1.0
+    m, ex = np.frexp(amax)                    # amax = m 2^ex; 448 = 0.875 2^9
+    return float(np.ldexp(1.0, int(ex) - 9 + (1 if m > 0.875 else 0)))
+
+
+def fp8_block_quantize(x, block: int = FP8_BLOCK):
+    """x [rows, cols] (cols a multiple of block) -> (q, scales): q the E4M3
+    values of x / scale, scales [rows, cols / block]."""
+    x = _f64(x)
+    rows, cols = x.shape
+    nb = cols // block
+    scales = np.ones((rows, nb))
+    q = np.zeros_like(x)
+    for r in range(rows):
+        for b in range(nb):
+            blk = x[r, b * block:(b + 1) * block]
+            sc = fp8_block_scale(np.max(np.abs(blk)))
+            scales[r, b] = sc
+            q[r, b * block:(b + 1) * block] = e4m3_round(blk / sc)
+    return q, scales
+
+
+def fp8_block_dequantize(q, scales, block: int = FP8_BLOCK) -> np.ndarray:
+    """q * scale, the scale repeated over its block."""
+    return _f64(q) * np.repeat(_f64(scales), block, axis=1)
+
+
+# --------------------------------------------------------------------------
 # Whole layer
 # --------------------------------------------------------------------------
 
@@ -232,28 +294,38 @@ def layer_forward(inp: dict, k: int | None = None, idx=None) -> dict:
                 y_perm=y_perm, y_sh=y_sh, y_lat=y_lat, out=out)
 
 
-def swiglu_expert_backward(zrows, W13e, W2e, d_o):
+def swiglu_expert_backward(zrows, W13e, W2e, d_o, gu_cache=None):
     """Chain rule through o = (silu(g) * u) W2, [g|u] = z W13.
-    Returns dz, dW13e, dW2e."""
+    Returns dz, dW13e, dW2e.
+
+    gu_cache = (g~, u~): the backward's g and u come from a cache of the
+    forward's values (the FP8 cache of [SWAP], see fp8_block_quantize) in the
+    SwiGLU derivative; h, the down projection's input, is the forward's own
+    (reading: the cache holds the GMM output [g|u]; h is kept as it is)."""
     zrows, W13e, W2e = _f64(zrows), _f64(W13e), _f64(W2e)
     f = W2e.shape[0]
     gu = zrows @ W13e
     g, u = gu[:, :f], gu[:, f:]
-    sg = 1.0 / (1.0 + np.exp(-g))
-    silu = g * sg
-    h = silu * u
+    h = _silu(g) * u
     dW2e = h.T @ d_o
     dh = d_o @ W2e.T
+    if gu_cache is not None:
+        g, u = _f64(gu_cache[0]), _f64(gu_cache[1])
+    sg = 1.0 / (1.0 + np.exp(-g))
+    silu = g * sg
     dg = dh * u * sg * (1.0 + g * (1.0 - sg))     # d silu / dg = s (1 + g (1 - s))
     du = dh * silu
     dgu = np.concatenate([dg, du], axis=1)
     return dgu @ W13e.T, zrows.T @ dgu, dW2e
 
 
-def layer_backward(inp: dict, fwd: dict, dout=None) -> dict:
+def layer_backward(inp: dict, fwd: dict, dout=None, fp8_cache: bool = False) -> dict:
     """Gradients of loss = sum(out * dout) (dout defaults to inp["g"]) with
     respect to x and every weight, routing held at its forward choice (the
     selection is piecewise constant; the router bias is a constant).
+    fp8_cache: the routed experts' backward takes g and u from their FP8 block
+    cache (fp8_block_quantize of each expert's g and u, [SWAP]); the shared
+    experts keep theirs exact.
 
     Returns dx, dWr, dW_dn, dW13, dW2, dW13_sh, dW2_sh, dW_up and the routing
     weight gradient d_w [T,k] (fp64)."""
@@ -278,11 +350,14 @@ def layer_backward(inp: dict, fwd: dict, dout=None) -> dict:
         a, b = int(offsets[e]), int(offsets[e + 1])
         if b == a:
             continue                                   # empty expert: zero gradient
-        o = swiglu_expert(z_perm[a:b], inp["W13"][e], inp["W2"][e])
+        o, ge, ue, _ = swiglu_expert(z_perm[a:b], inp["W13"][e], inp["W2"][e], True)
         d_row_w[a:b] = np.einsum("rc,rc->r", dy_perm[a:b], o)
         d_o = dy_perm[a:b] * row_w[a:b, None]
+        cache = None
+        if fp8_cache:
+            cache = tuple(fp8_block_dequantize(*fp8_block_quantize(v)) for v in (ge, ue))
         dz_perm[a:b], dW13[e], dW2[e] = swiglu_expert_backward(z_perm[a:b], inp["W13"][e],
-                                                         inp["W2"][e], d_o)
+                                                         inp["W2"][e], d_o, cache)
     S = inp["W13_sh"].shape[0]
     dz = np.zeros_like(z)
     dW13_sh = np.zeros((S,) + tuple(inp["W13_sh"].shape[1:]))
