@@ -206,11 +206,11 @@ def combine(y_perm, slot_of, y_shared=None):
 # FP8 E4M3 (4 exponent bits with bias 7, 3 mantissa bits, subnormals, largest
 # finite value 448, no infinities), round to nearest with ties to the even
 # mantissa, saturating at +-448; one power-of-two scale per row and block of
-# FP8_BLOCK consecutive columns, the smallest that brings the block's largest
-# magnitude to at most 448 (power of two: scaling is exact, so the rounding
-# decisions depend on the values alone).
+# FP8_BLOCK = 64 consecutive columns of g (and of u), the smallest that brings
+# the block's largest magnitude to at most 448 (power of two: scaling is exact,
+# so the rounding decisions depend on the values alone).
 
-FP8_BLOCK = 128
+FP8_BLOCK = 64
 E4M3_MAX = 448.0
 
 
