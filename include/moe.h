@@ -18,6 +18,10 @@
  *             counted from the current routing result.
  *   [GGEMM]   same page, section "权重预取与梯度归约": one Grouped GEMM runs all
  *             experts of a device through a unified compute view.
+ *   [SWAP]    the [OPS] page, section "Swap Core:算子级精准缓存与异步 Offload 协同,
+ *             训练性能提升 15%": outputs of selected MatMul/GMM operators are cached
+ *             for the backward, optionally compressed by FP8 activation
+ *             quantization and dequantization.
  * Where the pages are silent the library takes these readings: the router is
  * sigmoid(x @ Wr (+ bias)) on the model-width input, the k largest logits are
  * selected (lower expert id wins a tie) and their sigmoids renormalised to sum
@@ -214,6 +218,20 @@ int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16
                        int E, int R, int l, int f, uint16_t* gu_save, uint16_t* h,
                        uint16_t* y_perm, void* stream);
 
+/* moe_grouped_swiglu with the GMM output [g|u] cached for the backward in FP8
+ * ([SWAP]) instead of bf16: E4M3 (round to nearest even, saturating at +-448)
+ * of g / s and u / s, with one power-of-two scale s per row and 64-feature block,
+ * the smallest with max |block| <= 448 s (1 when that maximum is below 2^-100):
+ *   gu8[r][c]               E4M3 bytes [R][2f] (columns as in gu_save)
+ *   gu_scale[r][b]          fp32 [R][2f/64]: blocks of g (b < f/64), then of u
+ * h and y_perm are exactly those of moe_grouped_swiglu. f must be a multiple of
+ * 128 (MOE_ERR_UNSUPPORTED otherwise); gu8 16-byte aligned. The cache takes 1 + 1/16
+ * bytes per value instead of 2. */
+int moe_grouped_swiglu_fp8cache(const uint16_t* z_perm, const uint16_t* W13, const uint16_t* W2,
+                                const int32_t* offsets, const int32_t* tile_sched,
+                                const float* row_w, int E, int R, int l, int f, uint8_t* gu8,
+                                float* gu_scale, uint16_t* h, uint16_t* y_perm, void* stream);
+
 /* Multi-bucket batching ("大模型落地昇腾" page, section "二、算力侧": experts with
  * similar token counts grouped into buckets, each with one batch shape), read
  * for this engine as an expert order: bucket class 0 for an empty expert, else
@@ -292,6 +310,18 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
                            int E, int R, int l, int f, uint16_t* dz_perm, float* d_row_w,
                            void* dW13, void* dW2, int wgrad_dtype, void* ws, size_t ws_bytes,
                            void* stream);
+
+/* moe_grouped_swiglu_bwd reading g and u from the FP8 cache of
+ * moe_grouped_swiglu_fp8cache (gu8 * scale of its block) in the SwiGLU
+ * derivative (dg, du); h, and with it dW2 and d_row_w, is the bf16 forward's
+ * as in moe_grouped_swiglu_bwd. Same workspace. */
+int moe_grouped_swiglu_bwd_fp8cache(const uint16_t* dy_perm, const uint16_t* z_perm,
+                                    const uint16_t* W13, const uint16_t* W2, const uint8_t* gu8,
+                                    const float* gu_scale, const uint16_t* h, const float* row_w,
+                                    const int32_t* offsets, const int32_t* tile_sched, int E,
+                                    int R, int l, int f, uint16_t* dz_perm, float* d_row_w,
+                                    void* dW13, void* dW2, int wgrad_dtype, void* ws,
+                                    size_t ws_bytes, void* stream);
 
 /* moe_grouped_swiglu_bwd with both permutes fused into the operand loads:
  * dy_perm[r] = dy_lat[token_of[r]] and z_perm[r] = z[token_of[r]] are gathered

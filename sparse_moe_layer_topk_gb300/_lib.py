@@ -51,6 +51,8 @@ SIGNATURES = {
     "moe_latent_proj": ([_P, _P, _I, _I, _I, _P, _P], _I),
     "moe_latent_proj_bwd": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P], _I),
     "moe_grouped_swiglu": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_grouped_swiglu_fp8cache": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P],
+                                    _I),
     "moe_grouped_swiglu_gather": ([_P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P],
                                   _I),
     "moe_grouped_swiglu_bwd_gather": ([_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
@@ -60,6 +62,8 @@ SIGNATURES = {
     "moe_unpermute_combine_bwd": ([_P, _P, _I, _I, _I, _P, _P], _I),
     "moe_grouped_swiglu_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                 _I, _P, _Z, _P], _I),
+    "moe_grouped_swiglu_bwd_fp8cache": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                         _P, _P, _P, _P, _I, _P, _Z, _P], _I),
     "moe_shared_swiglu_bwd": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _Z, _P],
                               _I),
     "moe_permute_bwd": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
@@ -202,6 +206,12 @@ def moe_grouped_swiglu(z_perm, W13, W2, offsets, tile_sched, row_w, E, R, l, f, 
           h, y_perm, stream)
 
 
+def moe_grouped_swiglu_fp8cache(z_perm, W13, W2, offsets, tile_sched, row_w, E, R, l, f, gu8,
+                                gu_scale, h, y_perm, stream=None):
+    _call("moe_grouped_swiglu_fp8cache", z_perm, W13, W2, offsets, tile_sched, row_w, E, R, l, f,
+          gu8, gu_scale, h, y_perm, stream)
+
+
 def moe_grouped_swiglu_gather(z, token_of, T, W13, W2, offsets, tile_sched, row_w, E, R, l, f,
                               gu_save, h, y_perm, stream=None):
     _call("moe_grouped_swiglu_gather", z, token_of, T, W13, W2, offsets, tile_sched, row_w, E, R,
@@ -233,6 +243,14 @@ def moe_grouped_swiglu_bwd(dy_perm, z_perm, W13, W2, gu_save, h, row_w, offsets,
                            stream=None):
     _call("moe_grouped_swiglu_bwd", dy_perm, z_perm, W13, W2, gu_save, h, row_w, offsets,
           tile_sched, E, R, l, f, dz_perm, d_row_w, dW13, dW2, wgrad_dtype, ws, ws_bytes, stream)
+
+
+def moe_grouped_swiglu_bwd_fp8cache(dy_perm, z_perm, W13, W2, gu8, gu_scale, h, row_w, offsets,
+                                    tile_sched, E, R, l, f, dz_perm, d_row_w, dW13, dW2,
+                                    wgrad_dtype, ws, ws_bytes, stream=None):
+    _call("moe_grouped_swiglu_bwd_fp8cache", dy_perm, z_perm, W13, W2, gu8, gu_scale, h, row_w,
+          offsets, tile_sched, E, R, l, f, dz_perm, d_row_w, dW13, dW2, wgrad_dtype, ws, ws_bytes,
+          stream)
 
 
 def moe_shared_swiglu_bwd(dy, z, W13_sh, W2_sh, gu_save, h, T, l, f, S, dz_sh, dW13_sh, dW2_sh,

@@ -298,17 +298,26 @@ namespace {
 
 // Grouped SwiGLU experts; A rows come from z_src ([src_rows][l]): permuted row r
 // is z_src row gather[r] when gather is given, else row r.
+// The FP8 cache of g|u (E4M3 bytes [R][2f] and fp32 scales [R][2f/64]) takes
+// the place of the bf16 gu_save when its pointers are given.
+struct Fp8Cache {
+  uint8_t* gu8 = nullptr;
+  float* scale = nullptr;
+};
+
 int grouped_swiglu_impl(const uint16_t* z_perm, long long src_rows, const int32_t* gather,
                         const uint16_t* W13, const uint16_t* W2, const int32_t* offsets,
                         const int32_t* tile_sched, const float* row_w, int E, int R, int l, int f,
                         uint16_t* gu_save, uint16_t* h, uint16_t* y_perm, void* stream,
-                        const int32_t* expert_order = nullptr) {
+                        const int32_t* expert_order = nullptr, Fp8Cache fp8 = Fp8Cache()) {
   MOE_REQUIRE(z_perm && W13 && W2 && offsets && tile_sched && h && y_perm, MOE_ERR_ARG);
   MOE_REQUIRE(E > 0 && R >= 0 && l > 0 && f > 0, MOE_ERR_ARG);
   MOE_REQUIRE(l % 64 == 0 && f % 64 == 0, MOE_ERR_ALIGN);
   MOE_REQUIRE(al16(z_perm) && al16(W13) && al16(W2) && al16(h) && al16(y_perm) &&
-                  (!gu_save || al16(gu_save)),
+                  (!gu_save || al16(gu_save)) && (!fp8.gu8 || al16(fp8.gu8)),
               MOE_ERR_ALIGN);
+  // the FP8 cache's 64-feature blocks are halves of the 128-feature n tiles
+  MOE_REQUIRE(!fp8.gu8 || (fp8.scale && f % 128 == 0 && !gu_save), MOE_ERR_UNSUPPORTED);
   if (R == 0) return MOE_OK;
   cudaStream_t st = S(stream);
   // GEMM1 + SwiGLU: [g|u] = z_perm W13[e]; h = silu(g) * u
@@ -338,6 +347,9 @@ int grouped_swiglu_impl(const uint16_t* z_perm, long long src_rows, const int32_
   L1.ldh = f;
   L1.gu = gu_save;
   L1.ldgu = 2ll * f;
+  L1.gu8 = fp8.gu8;
+  L1.gu_scale = fp8.scale;
+  L1.ld_scale = 2 * f / 64;
   MOE_CHECK(gemm_launch(L1, st));
   // GEMM2 + routing-weight scale: y_perm = row_w * (h W2[e])
   GemmLaunch L2;
@@ -373,6 +385,18 @@ int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16
                        uint16_t* y_perm, void* stream) {
   return grouped_swiglu_impl(z_perm, R, nullptr, W13, W2, offsets, tile_sched, row_w, E, R, l, f,
                              gu_save, h, y_perm, stream);
+}
+
+int moe_grouped_swiglu_fp8cache(const uint16_t* z_perm, const uint16_t* W13, const uint16_t* W2,
+                                const int32_t* offsets, const int32_t* tile_sched,
+                                const float* row_w, int E, int R, int l, int f, uint8_t* gu8,
+                                float* gu_scale, uint16_t* h, uint16_t* y_perm, void* stream) {
+  MOE_REQUIRE(gu8 && gu_scale, MOE_ERR_ARG);
+  Fp8Cache c;
+  c.gu8 = gu8;
+  c.scale = gu_scale;
+  return grouped_swiglu_impl(z_perm, R, nullptr, W13, W2, offsets, tile_sched, row_w, E, R, l, f,
+                             nullptr, h, y_perm, stream, nullptr, c);
 }
 
 int moe_expert_buckets(const int32_t* counts, int E, int32_t* expert_order,
@@ -483,15 +507,18 @@ int grouped_swiglu_bwd_impl(const uint16_t* dy_perm, const uint16_t* z_perm, lon
                             const uint16_t* gu_save, const uint16_t* h, const float* row_w,
                             const int32_t* offsets, const int32_t* tile_sched, int E, int R, int l,
                             int f, uint16_t* dz_perm, float* d_row_w, void* dW13, void* dW2,
-                            int wgrad_dtype, void* ws, size_t ws_bytes, void* stream) {
+                            int wgrad_dtype, void* ws, size_t ws_bytes, void* stream,
+                            Fp8Cache fp8 = Fp8Cache()) {
   MOE_REQUIRE(dy_perm && z_perm && W13 && W2 && h && offsets && tile_sched && dz_perm && d_row_w &&
                   dW13 && dW2,
               MOE_ERR_ARG);
-  MOE_REQUIRE(gu_save != nullptr, MOE_ERR_UNSUPPORTED);
+  MOE_REQUIRE((gu_save != nullptr) != (fp8.gu8 != nullptr), MOE_ERR_UNSUPPORTED);
+  MOE_REQUIRE(!fp8.gu8 || (fp8.scale && f % 64 == 0), MOE_ERR_UNSUPPORTED);
   MOE_REQUIRE(E > 0 && R >= 0 && l > 0 && f > 0, MOE_ERR_ARG);
   MOE_REQUIRE(wgrad_dtype == MOE_DTYPE_F32 || wgrad_dtype == MOE_DTYPE_BF16, MOE_ERR_ARG);
   MOE_REQUIRE(l % 64 == 0 && f % 64 == 0, MOE_ERR_ALIGN);
-  MOE_REQUIRE(al16(dy_perm) && al16(z_perm) && al16(W13) && al16(W2) && al16(gu_save) && al16(h) &&
+  MOE_REQUIRE(al16(dy_perm) && al16(z_perm) && al16(W13) && al16(W2) && al16(gu_save) &&
+                  al16(fp8.gu8) && al16(h) &&
                   al16(dz_perm) && al16(dW13) && al16(dW2),
               MOE_ERR_ALIGN);
   MOE_REQUIRE(ws != nullptr && ws_bytes >= grouped_bwd_ws(R, f), MOE_ERR_WORKSPACE);
@@ -531,6 +558,9 @@ int grouped_swiglu_bwd_impl(const uint16_t* dy_perm, const uint16_t* z_perm, lon
   D2.ldc = 2ll * f;
   D2.gu = const_cast<uint16_t*>(gu_save);
   D2.ldgu = 2ll * f;
+  D2.gu8 = fp8.gu8;
+  D2.gu_scale = fp8.scale;
+  D2.ld_scale = 2 * f / 64;
   D2.h = const_cast<uint16_t*>(h);
   D2.ldh = f;
   D2.row_w = row_w;
@@ -617,6 +647,22 @@ int moe_grouped_swiglu_bwd(const uint16_t* dy_perm, const uint16_t* z_perm, cons
   return grouped_swiglu_bwd_impl(dy_perm, z_perm, R, nullptr, W13, W2, gu_save, h, row_w, offsets,
                                  tile_sched, E, R, l, f, dz_perm, d_row_w, dW13, dW2, wgrad_dtype,
                                  ws, ws_bytes, stream);
+}
+
+int moe_grouped_swiglu_bwd_fp8cache(const uint16_t* dy_perm, const uint16_t* z_perm,
+                                    const uint16_t* W13, const uint16_t* W2, const uint8_t* gu8,
+                                    const float* gu_scale, const uint16_t* h, const float* row_w,
+                                    const int32_t* offsets, const int32_t* tile_sched, int E,
+                                    int R, int l, int f, uint16_t* dz_perm, float* d_row_w,
+                                    void* dW13, void* dW2, int wgrad_dtype, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  MOE_REQUIRE(gu8 && gu_scale, MOE_ERR_ARG);
+  Fp8Cache c;
+  c.gu8 = const_cast<uint8_t*>(gu8);
+  c.scale = const_cast<float*>(gu_scale);
+  return grouped_swiglu_bwd_impl(dy_perm, z_perm, R, nullptr, W13, W2, nullptr, h, row_w, offsets,
+                                 tile_sched, E, R, l, f, dz_perm, d_row_w, dW13, dW2, wgrad_dtype,
+                                 ws, ws_bytes, stream, c);
 }
 
 int moe_grouped_swiglu_bwd_gather(const uint16_t* dy_lat, const uint16_t* z,

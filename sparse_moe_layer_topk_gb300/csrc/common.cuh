@@ -418,6 +418,58 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// ---------------------------------------------------------------- FP8 (E4M3)
+
+// Two fp32 values -> an E4M3 pair (round to nearest even, saturating at
+// +-448), `lo` in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Sixteen fp32 values times `inv` -> sixteen E4M3 bytes (value i in byte i).
+__device__ __forceinline__ uint4 f32x16_to_e4m3(const float* v, float inv) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
+           (f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Four E4M3 values (the bytes of v, low byte first) -> fp32, exactly.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t v, float* out) {
+  asm("{\n\t.reg .b16 l, h, a0, a1, b0, b1;\n\t.reg .b32 pa, pb;\n\t"
+      "mov.b32 {l, h}, %4;\n\t"
+      "cvt.rn.f16x2.e4m3x2 pa, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 pb, h;\n\t"
+      "mov.b32 {a0, a1}, pa;\n\t"
+      "mov.b32 {b0, b1}, pb;\n\t"
+      "cvt.f32.f16 %0, a0;\n\t"
+      "cvt.f32.f16 %1, a1;\n\t"
+      "cvt.f32.f16 %2, b0;\n\t"
+      "cvt.f32.f16 %3, b1;\n\t}"
+      : "=f"(out[0]), "=f"(out[1]), "=f"(out[2]), "=f"(out[3])
+      : "r"(v));
+}
+
+// Block scale of the FP8 cache: the smallest power of two s with amax <= 448 s
+// (448 = 1.75 * 2^8, so the exponent comes from amax's bits with no rounding),
+// and 1 / s; s = 1 below 2^-100.
+__device__ __forceinline__ void fp8_block_scale(float amax, float& s, float& inv) {
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = static_cast<int>((b >> 23) & 0xFFu);
+  if (ef < 27) {
+    s = 1.0f;
+    inv = 1.0f;
+    return;
+  }
+  const int e = ef - 135 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  s = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+  inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
 // Epilogue sigmoid: s(x) = (1 + tanh(x / 2)) / 2 on the hardware tanh
 // approximation (one MUFU operation instead of an exponential and a
 // reciprocal; its error, a few 1e-4 at most, sits far below the bf16 rounding

@@ -72,6 +72,12 @@ struct GemmLaunch {
   const float* row_w = nullptr;
   void* gu = nullptr;  // bf16
   long long ldgu = 0;
+  // EPI_SWIGLU / EPI_SWIGLU_BWD with an FP8 cache of g|u instead of gu: E4M3
+  // bytes [rows][ldgu] and fp32 scales [rows][ld_scale], one per 64 features
+  // of g, then of u (ld_scale = 2 f / 64). The forward needs 256-wide tiles.
+  void* gu8 = nullptr;
+  float* gu_scale = nullptr;
+  int ld_scale = 0;
   void* h = nullptr;  // bf16
   long long ldh = 0;
   void* aux = nullptr;  // bf16

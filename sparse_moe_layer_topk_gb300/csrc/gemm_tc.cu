@@ -102,6 +102,12 @@ struct Params {
   const float* row_w;
   bf16* gu;
   long long ldgu;
+  // FP8 cache of g|u (instead of gu): E4M3 bytes [R][ldgu] and one fp32 scale
+  // per row and 64-feature block, gu_scale[row * ld_scale + block] (the f / 64
+  // g blocks, then the u blocks)
+  uint8_t* gu8;
+  float* gu_scale;
+  int ld_scale;
   bf16* h;
   long long ldh;
   bf16* aux;
@@ -803,10 +809,9 @@ struct StoreMaps {
 // SwiGLU-backward element math for eight columns: dh = w * acc,
 // dg = dh * u * s(g) * (1 + g (1 - s(g))), du = dh * silu(g), the routing-weight
 // dot acc . h, and w * h (the dW2 operand); bf16 in and out, fp32 math.
-__device__ __forceinline__ void swiglu_bwd8(const float* a, uint4 G, uint4 U, uint4 H, float w,
-                                            float& dot, uint4& DG, uint4& DU, uint4& HW) {
-  const uint32_t Gw[4] = {G.x, G.y, G.z, G.w};
-  const uint32_t Uw[4] = {U.x, U.y, U.z, U.w};
+__device__ __forceinline__ void swiglu_bwd8f(const float* a, const float* G, const float* U,
+                                             uint4 H, float w, float& dot, uint4& DG, uint4& DU,
+                                             uint4& HW) {
   const uint32_t Hw[4] = {H.x, H.y, H.z, H.w};
   uint32_t pdg[4], pdu[4], phw[4];
 #pragma unroll
@@ -815,8 +820,8 @@ __device__ __forceinline__ void swiglu_bwd8(const float* a, uint4 G, uint4 U, ui
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const float av = a[2 * e2 + hh];
-      const float gg = hh ? bf16_hi(Gw[e2]) : bf16_lo(Gw[e2]);
-      const float uu = hh ? bf16_hi(Uw[e2]) : bf16_lo(Uw[e2]);
+      const float gg = G[2 * e2 + hh];
+      const float uu = U[2 * e2 + hh];
       const float hv = hh ? bf16_hi(Hw[e2]) : bf16_lo(Hw[e2]);
       const float sg = sigmoidf_(gg);
       const float dh = w * av;
@@ -832,6 +837,22 @@ __device__ __forceinline__ void swiglu_bwd8(const float* a, uint4 G, uint4 U, ui
   DG = make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]);
   DU = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
   HW = make_uint4(phw[0], phw[1], phw[2], phw[3]);
+}
+
+// The same with g and u as bf16 (eight each, packed in pairs).
+__device__ __forceinline__ void swiglu_bwd8(const float* a, uint4 G, uint4 U, uint4 H, float w,
+                                            float& dot, uint4& DG, uint4& DU, uint4& HW) {
+  const uint32_t Gw[4] = {G.x, G.y, G.z, G.w};
+  const uint32_t Uw[4] = {U.x, U.y, U.z, U.w};
+  float gf[8], uf[8];
+#pragma unroll
+  for (int e2 = 0; e2 < 4; ++e2) {
+    gf[2 * e2] = bf16_lo(Gw[e2]);
+    gf[2 * e2 + 1] = bf16_hi(Gw[e2]);
+    uf[2 * e2] = bf16_lo(Uw[e2]);
+    uf[2 * e2 + 1] = bf16_hi(Uw[e2]);
+  }
+  swiglu_bwd8f(a, gf, uf, H, w, dot, DG, DU, HW);
 }
 
 // SwiGLU-backward epilogue with TMA-staged inputs. Each of the 4 epilogue
@@ -890,9 +911,16 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
     const int slot = static_cast<int>(issued % NS);
     if (lane == 0) {
       const uint32_t d = smem_u32(slots + slot * SLOT);
-      mbar_arrive_expect_tx(&lb[slot], SLOT);
-      tma_load_2d(d, sm.ld_gu, &lb[slot], gcol, row0);
-      tma_load_2d(d + 2048, sm.ld_gu, &lb[slot], gcol + p.f, row0);
+      if (p.gu8) {
+        // FP8 cache: 32-byte rows of g and u at 0 and 1024, h at 4096
+        mbar_arrive_expect_tx(&lb[slot], 1024 + 1024 + 2048);
+        tma_load_2d(d, sm.ld_gu, &lb[slot], gcol, row0);
+        tma_load_2d(d + 1024, sm.ld_gu, &lb[slot], gcol + p.f, row0);
+      } else {
+        mbar_arrive_expect_tx(&lb[slot], SLOT);
+        tma_load_2d(d, sm.ld_gu, &lb[slot], gcol, row0);
+        tma_load_2d(d + 2048, sm.ld_gu, &lb[slot], gcol + p.f, row0);
+      }
       tma_load_2d(d + 4096, sm.ld_h, &lb[slot], n, row0);
     }
     ++issued;
@@ -945,13 +973,47 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
         uint8_t* const sl = slots + slot * SLOT;
         uint8_t* const rowp = sl + lane * 64;
         bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + gcol;
+        // FP8 cache: the lane's 32 g and 32 u bytes (rows of 32 bytes) are read
+        // before any lane writes its outputs over them; block scales per row
+        uint32_t g8[8], u8[8];
+        float sgl = 1.0f, sul = 1.0f;
+        if (p.gu8) {
+          const uint4* const gp = reinterpret_cast<const uint4*>(sl + lane * 32);
+          const uint4* const up = reinterpret_cast<const uint4*>(sl + 1024 + lane * 32);
+          const uint4 g0 = gp[0], g1 = gp[1], u0 = up[0], u1 = up[1];
+          g8[0] = g0.x; g8[1] = g0.y; g8[2] = g0.z; g8[3] = g0.w;
+          g8[4] = g1.x; g8[5] = g1.y; g8[6] = g1.z; g8[7] = g1.w;
+          u8[0] = u0.x; u8[1] = u0.y; u8[2] = u0.z; u8[3] = u0.w;
+          u8[4] = u1.x; u8[5] = u1.y; u8[6] = u1.z; u8[7] = u1.w;
+          if (row_ok) {
+            const float* const sc = p.gu_scale + grow * p.ld_scale + (n - sx * p.f) / 64;
+            sgl = __ldg(sc);
+            sul = __ldg(sc + p.ld_scale / 2);
+          }
+          __syncwarp();
+        }
 #pragma unroll
         for (int vv = 0; vv < 4; ++vv) {
           const int off = (vv ^ sw) << 4;
           uint4 DG, DU, HW;
-          swiglu_bwd8(a + 8 * vv, *reinterpret_cast<const uint4*>(rowp + off),
-                      *reinterpret_cast<const uint4*>(rowp + 2048 + off),
-                      *reinterpret_cast<const uint4*>(rowp + 4096 + off), w, dot, DG, DU, HW);
+          if (p.gu8) {
+            float gf[8], uf[8];
+            e4m3x4_to_f32(g8[2 * vv], gf);
+            e4m3x4_to_f32(g8[2 * vv + 1], gf + 4);
+            e4m3x4_to_f32(u8[2 * vv], uf);
+            e4m3x4_to_f32(u8[2 * vv + 1], uf + 4);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              gf[i] *= sgl;
+              uf[i] *= sul;
+            }
+            swiglu_bwd8f(a + 8 * vv, gf, uf, *reinterpret_cast<const uint4*>(rowp + 4096 + off),
+                         w, dot, DG, DU, HW);
+          } else {
+            swiglu_bwd8(a + 8 * vv, *reinterpret_cast<const uint4*>(rowp + off),
+                        *reinterpret_cast<const uint4*>(rowp + 2048 + off),
+                        *reinterpret_cast<const uint4*>(rowp + 4096 + off), w, dot, DG, DU, HW);
+          }
           if (use_tma) {
             *reinterpret_cast<uint4*>(rowp + off) = DG;
             *reinterpret_cast<uint4*>(rowp + 2048 + off) = DU;
@@ -1018,6 +1080,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   int slot_bytes;
   if (p.epi == EPI_STORE) slot_bytes = p.c_bf16 ? 2048 : 4096;
   else if (p.epi == EPI_ROWSCALE) slot_bytes = 2048;
+  else if (p.gu8) slot_bytes = 2048;  // EPI_SWIGLU, FP8 cache: h, g and u of 16 columns
   else slot_bytes = (CW16 ? 1024 : 2048) * (p.gu ? 3 : 1);  // EPI_SWIGLU
   int nslots = Cfg<BN, EW, CW16>::STG / slot_bytes;
   if (nslots > 4) nslots = 4;
@@ -1119,8 +1182,37 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
         // TMEM columns [0, BN/2) hold the gate, [BN/2, BN) the up projection;
         // 16-column chunks, the two warps of a lane quadrant taking turns.
         const int out_batch = (p.b_batch_mode == BATCH_FROM_N) ? ti.batch : 0;
+        // FP8 cache: each warp takes a contiguous half of the tile's features
+        // (a 64-feature block of g and one of u per row) so that it alone sees
+        // the block's largest |g| and |u|; one scale per row and block.
+        const int c_lo = p.gu8 ? grp * (BN / 32 / NG) : grp;
+        const int c_hi = p.gu8 ? c_lo + BN / 32 / NG : BN / 32;
+        const int c_step = p.gu8 ? 1 : NG;
+        float inv_g = 1.0f, inv_u = 1.0f;
+        if (p.gu8) {
+          float ag = 0.0f, au = 0.0f;
 #pragma unroll 1
-        for (int c = grp; c < BN / 32; c += NG) {
+          for (int c = c_lo; c < c_hi; ++c) {
+            float g[16], u[16];
+            ld_chunk16(trow + c * 16, g);
+            ld_chunk16(trow + BN / 2 + c * 16, u);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              ag = fmaxf(ag, fabsf(g[i]));
+              au = fmaxf(au, fabsf(u[i]));
+            }
+          }
+          float sg, su;
+          fp8_block_scale(ag, sg, inv_g);
+          fp8_block_scale(au, su, inv_u);
+          if (row_ok) {
+            float* const sc = p.gu_scale + grow * p.ld_scale + (ti.nb0 + c_lo * 16) / 64;
+            sc[0] = sg;
+            sc[p.ld_scale / 2] = su;
+          }
+        }
+#pragma unroll 1
+        for (int c = c_lo; c < c_hi; c += c_step) {
           float g[16], u[16], hv[16];
           ld_chunk16(trow + c * 16, g);
           ld_chunk16(trow + BN / 2 + c * 16, u);
@@ -1132,14 +1224,20 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           if (use_tma) {
             stage_begin();
             stage_bf16_16(stg, lane, hv);
-            if (p.gu) {
+            if (p.gu8) {
+              *reinterpret_cast<uint4*>(stg + 1024 + lane * 16) = f32x16_to_e4m3(g, inv_g);
+              *reinterpret_cast<uint4*>(stg + 1536 + lane * 16) = f32x16_to_e4m3(u, inv_u);
+            } else if (p.gu) {
               stage_bf16_16(stg + 1024, lane, g);
               stage_bf16_16(stg + 2048, lane, u);
             }
             stage_end();
             if (lane == 0) {
               tma_store_2d(sm.c0, stg_s, hcol, row0);
-              if (p.gu) {
+              if (p.gu8) {
+                tma_store_2d(sm.c1, stg_s + 1024, gcol, row0);
+                tma_store_2d(sm.c1, stg_s + 1536, gcol + p.f, row0);
+              } else if (p.gu) {
                 tma_store_2d(sm.c1, stg_s + 1024, gcol, row0);
                 tma_store_2d(sm.c1, stg_s + 2048, gcol + p.f, row0);
               }
@@ -1148,7 +1246,10 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             pending = true;
           } else if (row_ok) {
             store_bf16_row16(p.h + grow * p.ldh + hcol, hv);
-            if (p.gu) {
+            if (p.gu8) {
+              store16(p.gu8 + grow * p.ldgu + gcol, f32x16_to_e4m3(g, inv_g));
+              store16(p.gu8 + grow * p.ldgu + gcol + p.f, f32x16_to_e4m3(u, inv_u));
+            } else if (p.gu) {
               store_bf16_row16(p.gu + grow * p.ldgu + gcol, g);
               store_bf16_row16(p.gu + grow * p.ldgu + gcol + p.f, u);
             }
@@ -1412,6 +1513,20 @@ bool make_store_map(CUtensorMap* map, void* ptr, bool f32, bool rank3, long long
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map of a byte matrix [d1][d0] (ld bytes between rows) for 32-row boxes
+// of box_cols bytes (16 or 32), no swizzle: the FP8 cache's blocks.
+bool make_u8_map(CUtensorMap* map, void* ptr, long long d0, long long d1, long long ld,
+                 int box_cols) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int BN, int EW, bool CW16, bool PAIR, int GW = 0, bool SBWD = false>
 int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   using C = Cfg<BN, EW, CW16, PAIR, SBWD>;
@@ -1467,6 +1582,16 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
   p.row_w = L.row_w;
   p.gu = reinterpret_cast<bf16*>(L.gu);
   p.ldgu = L.ldgu;
+  p.gu8 = static_cast<uint8_t*>(L.gu8);
+  p.gu_scale = L.gu_scale;
+  p.ld_scale = L.ld_scale;
+  if (L.gu8) {
+    // one scale per 64 features: a forward epilogue warp holds 64 of a 256-wide tile's
+    if (!L.gu_scale || L.ld_scale <= 0 || L.gu ||
+        (L.epi == EPI_SWIGLU && !(BN == 256 && EW == 8 && CW16)) ||
+        (L.epi != EPI_SWIGLU && L.epi != EPI_SWIGLU_BWD))
+      return MOE_ERR_UNSUPPORTED;
+  }
   p.h = reinterpret_cast<bf16*>(L.h);
   p.ldh = L.ldh;
   p.aux = reinterpret_cast<bf16*>(L.aux);
@@ -1555,14 +1680,16 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
     ok = make_store_map(&mapC0, L.h, false, false, L.ldh, rows_out, 1, L.ldh, 0, 16);
     if (ok && L.gu)
       ok = make_store_map(&mapC1, L.gu, false, false, L.ldgu, rows_out, 1, L.ldgu, 0, 16);
+    if (ok && L.gu8) ok = make_u8_map(&mapC1, L.gu8, L.ldgu, rows_out, L.ldgu, 16);
   } else if (L.epi == EPI_ROWSCALE) {
     ok = make_store_map(&mapC0, L.C, false, false, L.N, rows_out, 1, L.ldc, 0);
   } else {  // EPI_SWIGLU_BWD (32-column blocks)
     ok = make_store_map(&mapC0, L.C, false, false, L.ldc, rows_out, 1, L.ldc, 0);
     if (ok && L.aux)
       ok = make_store_map(&mapC1, L.aux, false, false, L.ldaux, rows_out, 1, L.ldaux, 0);
-    // the epilogue's inputs g|u and h, loaded in the same 32 x 32 blocks
-    if (ok) ok = make_store_map(&mapA2, L.gu, false, false, L.ldgu, rows_out, 1, L.ldgu, 0);
+    // the epilogue's inputs g|u (or their FP8 cache) and h, in the same 32 x 32 blocks
+    if (ok && L.gu8) ok = make_u8_map(&mapA2, L.gu8, L.ldgu, rows_out, L.ldgu, 32);
+    else if (ok) ok = make_store_map(&mapA2, L.gu, false, false, L.ldgu, rows_out, 1, L.ldgu, 0);
     if (ok) ok = make_store_map(&mapB2, L.h, false, false, L.ldh, rows_out, 1, L.ldh, 0);
   }
   if (!ok) return MOE_ERR_ARG;

@@ -16,6 +16,11 @@ gather their permuted rows from z and dy_lat themselves
 saves ~1 GB of activations and ~2 GB of DRAM traffic at T=16384 but is slower
 on GB300 (the row copies keep fewer bytes in flight per SM than the tiled TMA
 loads of the permuted tensors), so the default is the explicit permute.
+
+With fp8_cache the routed experts' GMM output [g|u] is kept for the backward
+as E4M3 with one scale per row and 64 features (moe_grouped_swiglu[_bwd]_fp8cache)
+instead of bf16: 1 + 1/16 bytes per value instead of 2, and the backward's
+SwiGLU derivative reads the dequantized values.
 """
 from __future__ import annotations
 
@@ -28,9 +33,13 @@ BF16 = torch.bfloat16
 
 class LatentMoELayer:
     def __init__(self, weights: dict, T: int, k: int, wgrad_dtype: int = M.MOE_DTYPE_F32,
-                 device="cuda", fused_gather: bool = False, aux_scale: float = 0.0):
+                 device="cuda", fused_gather: bool = False, aux_scale: float = 0.0,
+                 fp8_cache: bool = False):
+        if fp8_cache and fused_gather:
+            raise ValueError("fp8_cache runs with the explicit permute")
         self.w = weights
         self.fused_gather = fused_gather
+        self.fp8_cache = fp8_cache
         self.aux_scale = aux_scale  # > 0: add aux_scale * the auxiliary balance loss
         self.T = T
         self.k = k
@@ -56,7 +65,9 @@ class LatentMoELayer:
         self.token_of = e(R, dt=torch.int32)
         self.row_w = e(R, dt=torch.float32)
         self.z_perm = None if fused_gather else e(R, l)
-        self.gu = e(R, 2 * f)
+        self.gu = None if fp8_cache else e(R, 2 * f)
+        self.gu8 = e(R, 2 * f, dt=torch.uint8) if fp8_cache else None
+        self.gu_scale = e(R, 2 * f // 64, dt=torch.float32) if fp8_cache else None
         self.h = e(R, f)
         self.y_perm = e(R, l)
         self.gu_sh = e(T_, S * 2 * f)
@@ -115,6 +126,10 @@ class LatentMoELayer:
             M.moe_grouped_swiglu_gather(self.z, self.token_of, T, w["W13"], w["W2"], self.offsets,
                                         self.tile_sched, self.row_w, E, R, l, f, self.gu, self.h,
                                         self.y_perm, stream)
+        elif self.fp8_cache:
+            M.moe_grouped_swiglu_fp8cache(self.z_perm, w["W13"], w["W2"], self.offsets,
+                                          self.tile_sched, self.row_w, E, R, l, f, self.gu8,
+                                          self.gu_scale, self.h, self.y_perm, stream)
         else:
             M.moe_grouped_swiglu(self.z_perm, w["W13"], w["W2"], self.offsets, self.tile_sched,
                                  self.row_w, E, R, l, f, self.gu, self.h, self.y_perm, stream)
@@ -138,6 +153,13 @@ class LatentMoELayer:
                                             self.tile_sched, E, R, l, f, self.dz_perm,
                                             self.d_row_w, g["W13"], g["W2"], wd, self.ws["gbwd"],
                                             self.ws_sizes["gbwd"], stream)
+        elif self.fp8_cache:
+            M.moe_unpermute_combine_bwd(self.dy_lat, self.token_of, T, k, l, self.dy_perm, stream)
+            M.moe_grouped_swiglu_bwd_fp8cache(self.dy_perm, self.z_perm, w["W13"], w["W2"],
+                                              self.gu8, self.gu_scale, self.h, self.row_w,
+                                              self.offsets, self.tile_sched, E, R, l, f,
+                                              self.dz_perm, self.d_row_w, g["W13"], g["W2"], wd,
+                                              self.ws["gbwd"], self.ws_sizes["gbwd"], stream)
         else:
             M.moe_unpermute_combine_bwd(self.dy_lat, self.token_of, T, k, l, self.dy_perm, stream)
             M.moe_grouped_swiglu_bwd(self.dy_perm, self.z_perm, w["W13"], w["W2"], self.gu,
