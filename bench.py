@@ -460,7 +460,8 @@ def _event_time(fn, steps, warmup, stream):
 
 def secondary_workloads(steps, warmup, tc_peak):
     """Forward-only tokens/s at T=4096 (uniform and Zipf-skewed routing), the
-    bench step with bf16 weight gradients, and the expert-parallel rank workload (grouped SwiGLU GEMMs + return to arrival
+    bench step with bf16 weight gradients and with the FP8 cache of g|u, and the
+    expert-parallel rank workload (grouped SwiGLU GEMMs + return to arrival
     order, 14 experts x 65536 rows), each timed with CUDA events after warm-up.
     Returns a dict for the JSON line."""
     import numpy as np
@@ -511,6 +512,24 @@ def secondary_workloads(steps, warmup, tc_peak):
     ms = _event_time(graph.replay, steps, warmup, stream)
     out[cfg.name + "_bf16_wgrad"] = {"ms_per_step": round(ms, 4),
                                       "tokens_per_s": cfg.T / (ms / 1000.0)}
+    del graph, layer
+    torch.cuda.empty_cache()
+    # the bench step with the routed experts' g|u cached in FP8 for the backward
+    layer = LatentMoELayer(weights_to_device(inp), cfg.T, cfg.k, M.MOE_DTYPE_F32, fp8_cache=True)
+    layer.step(x, g)
+    graph = layer.capture_step(x, g)
+    ms = _event_time(graph.replay, steps, warmup, stream)
+    M.moe_timing_report()
+    M.moe_timing_enable(True)
+    _event_time(lambda: layer.step(x, g), steps, 0, stream)
+    M.moe_timing_enable(False)
+    per = M.moe_timing_report()
+    R, f = cfg.T * cfg.k, cfg.f
+    out[cfg.name + "_fp8_cache"] = {
+        "ms_per_step": round(ms, 4), "tokens_per_s": cfg.T / (ms / 1000.0),
+        "gu_cache_bytes": R * 2 * f + R * (2 * f // 64) * 4, "gu_bf16_bytes": R * 2 * f * 2,
+        "kernels_us": {n: round(per[n][1] / per[n][0] * 1000.0, 2)
+                       for n in ("expert_gemm1_swiglu", "expert_dgrad2_swiglu_bwd") if n in per}}
     del graph, layer, inp, x, g
     torch.cuda.empty_cache()
     ep = I.make_ep_rank_inputs()

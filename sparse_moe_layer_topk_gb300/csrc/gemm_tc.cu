@@ -935,6 +935,31 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
     const Tile ti = tile_of<BN, PAIR>(p, ttab, it, t);
     const int buf = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
+    // FP8 cache: the lane's row scales for the tile's 64-column blocks, requested
+    // before the accumulator wait so that they arrive while it lasts
+    static_assert(BN / 64 <= 4, "four scale blocks per tile at most");
+    float4 sgq = make_float4(1.0f, 1.0f, 1.0f, 1.0f), suq = sgq;
+    if (p.gu8) {
+      const int qr0 = quad_rows(p, ti.rows);
+      const int rl = q * qr0 + static_cast<int>(lane);
+      const bool rok = static_cast<int>(lane) < qr0 && rl < ti.rows;
+      const float* const sc =
+          p.gu_scale + static_cast<long long>(ti.m0 + rl) * p.ld_scale + ti.nb0 / 64;
+      auto ld = [&](int i, int off) {
+        return (rok && ti.nb0 + 64 * i < p.N) ? __ldg(sc + off + i) : 1.0f;
+      };
+      const int uo = p.ld_scale / 2;
+      sgq.x = ld(0, 0);
+      suq.x = ld(0, uo);
+      sgq.y = ld(1, 0);
+      suq.y = ld(1, uo);
+      if (BN / 64 > 2) {
+        sgq.z = ld(2, 0);
+        suq.z = ld(2, uo);
+        sgq.w = ld(3, 0);
+        suq.w = ld(3, uo);
+      }
+    }
     if (!mbar_wait<PAIR>(&tfull[buf], use & 1u, abort_flag)) {
       raise_abort(abort_flag, p.err_flag);
       break;
@@ -985,11 +1010,9 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
           g8[4] = g1.x; g8[5] = g1.y; g8[6] = g1.z; g8[7] = g1.w;
           u8[0] = u0.x; u8[1] = u0.y; u8[2] = u0.z; u8[3] = u0.w;
           u8[4] = u1.x; u8[5] = u1.y; u8[6] = u1.z; u8[7] = u1.w;
-          if (row_ok) {
-            const float* const sc = p.gu_scale + grow * p.ld_scale + (n - sx * p.f) / 64;
-            sgl = __ldg(sc);
-            sul = __ldg(sc + p.ld_scale / 2);
-          }
+          const int bi = c >> 1;  // the chunk's 64-column block within the tile
+          sgl = bi == 0 ? sgq.x : bi == 1 ? sgq.y : bi == 2 ? sgq.z : sgq.w;
+          sul = bi == 0 ? suq.x : bi == 1 ? suq.y : bi == 2 ? suq.z : suq.w;
           __syncwarp();
         }
 #pragma unroll
