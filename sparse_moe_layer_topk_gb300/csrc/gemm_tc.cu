@@ -214,8 +214,10 @@ __device__ __forceinline__ Tile decode(const Params& p, int t) {
     const int per = mtx * p.nt;
     ti.g = t / per;
     t -= ti.g * per;
-    ti.n_blk = t / mtx;
-    int m_blk = t - ti.n_blk * mtx;
+    // n fastest: the n tiles of one row block run side by side, so an A larger
+    // than L2 (read by each of them) comes from DRAM once
+    int m_blk = t / p.nt;
+    ti.n_blk = t - m_blk * p.nt;
     if (PAIR) m_blk = 2 * m_blk + static_cast<int>(cluster_ctarank());
     ti.m0 = m_blk * BM;
     ti.rows = min(BM, p.M - ti.m0);
