@@ -44,7 +44,7 @@ Cached g_cache[kMaxDevices] = {};
 PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
 std::once_flag g_ctx_once;
 
-// The driver's current context (nullptr when it cannot be queried).
+// The CUDA driver API's current context (nullptr when it cannot be queried).
 CUcontext current_context() {
   std::call_once(g_ctx_once, []() {
     cudaDriverEntryPointQueryResult q;

@@ -140,7 +140,7 @@ def test_clock_samples_parsing():
     out = "\n".join([
         "2070, 2070, 910.55, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
         "2055, 2070, 1398.20, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
-        "[N/A], 2070, [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]",   # a sample the driver could not read
+        "[N/A], 2070, [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]",   # a sample nvidia-smi could not read
         "2040, 2070, 1401.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
         "garbage",
     ])
