@@ -107,6 +107,7 @@ def kernel_work(cfg, T, wgrad_bytes=4):
     weight gradients are written as fp32 (wgrad_bytes=4) or bf16 (2)."""
     d, l, E, k, S, f = cfg.d, cfg.l, cfg.E, cfg.k, cfg.S, cfg.f
     R = T * k
+    nch = (T + 255) // 256  # token chunks of the routing-map kernels
     w13 = E * l * 2 * f * 2
     w2 = E * f * l * 2
     b = 2  # bf16 bytes
@@ -147,7 +148,40 @@ def kernel_work(cfg, T, wgrad_bytes=4):
         "down_proj_router_dgrad": (2 * T * d * l + 2 * T * k * d,
                                    T * l * b + d * l * b + T * k * 6 + d * E * b + T * d * b),
         "router_wgrad": (2 * T * k * d, T * d * b + T * k * 6 + d * E * g),
+        # routing maps: the per-chunk expert histogram (chunks of 256 tokens) is
+        # this design's intermediate; hist reads the ids, scan turns the
+        # histogram into per-chunk prefixes plus counts / offsets / schedule, maps
+        # reads ids, weights and prefixes and writes slot_of, token_of and row_w
+        "permute_hist": (0, R * 4 + nch * E * 4),
+        "permute_scan": (0, 2 * nch * E * 4 + 3 * (E + 1) * 4),
+        "permute_maps": (0, 2 * R * 4 + nch * E * 4 + E * 4 + 3 * R * 4),
+        # the shared experts' K-split weight gradients: each launch reads its
+        # slices' fp32 partials and writes the gradient (mean of the two launches)
+        "splitk_reduce": (0, sum(m * n * (4 * s + g) for m, n, s in splitk_shapes(cfg, T)) // 2),
     }
+
+
+def pick_bn(n):
+    """Tile width of the GEMM engine for an N-wide output: 256 unless N is narrow or
+    a 256-wide tail would waste more than a quarter."""
+    return 256 if (n % 256 == 0 or (n > 512 and n % 256 >= 128)) else 128
+
+
+def wgrad_splitk(m, n, kdim):
+    """K slices of a dense weight gradient with few output tiles, as the library
+    chooses them: enough for ~128 tiles, at most 4, each slice >= 1024 rows of K."""
+    tiles = ((m + 127) // 128) * ((n + pick_bn(n) - 1) // pick_bn(n))
+    s = 1
+    while s < 4 and tiles * s * 2 <= 128 and kdim // (s * 2) >= 1024:
+        s *= 2
+    return s
+
+
+def splitk_shapes(cfg, T):
+    """(M, N, slices) of the shared experts' two weight gradients: dW2_sh [S f][l]
+    and dW13_sh [l][S 2f], K = T."""
+    sf, l = cfg.S * cfg.f, cfg.l
+    return [(sf, l, wgrad_splitk(sf, l, T)), (l, 2 * sf, wgrad_splitk(l, 2 * sf, T))]
 
 
 def dense_executed_flops(cfg, T):

@@ -194,6 +194,17 @@ class LatentMoELayer:
             self.step(x, dout)
         return g
 
+    def capture_halves(self, x, dout):
+        """The forward on x and the backward on dout as two CUDA graphs, so that
+        a step may start before its dout has arrived."""
+        gf = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf):
+            self.forward(x)
+        gb = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gb):
+            self.backward(dout)
+        return gf, gb
+
     def steps_from_host(self, x_host, g_host, dx_host, graphs: bool = True):
         """Forward + backward for each (x, dout) pair of pinned host tensors,
         writing each step's input gradient back to the pinned dx_host[i].
@@ -202,8 +213,9 @@ class LatentMoELayer:
         run on their own streams (separate copy engines) while step i computes;
         device inputs and input gradients are double-buffered and ordered with
         events, so every step still copies its own inputs in and its gradient
-        out. With graphs, each slot's step is a CUDA graph captured on first
-        use. Returns after the last copy has been enqueued; synchronise the
+        out. A step's forward waits for its x alone and its backward for its
+        dout, which is copied in after x. With graphs, each slot's forward and
+        backward are CUDA graphs captured on first use. Returns after the last copy has been enqueued; synchronise the
         current stream's device to wait for the results."""
         n = len(x_host)
         assert len(g_host) == n and len(dx_host) == n
@@ -223,10 +235,11 @@ class LatentMoELayer:
             self._pipe_graphs = []
             for s in range(2):
                 self.dx = P["dx"][s]
-                self._pipe_graphs.append(self.capture_step(P["x"][s], P["g"][s]))
+                self._pipe_graphs.append(self.capture_halves(P["x"][s], P["g"][s]))
             self.dx = keep
         ev = lambda: torch.cuda.Event()  # noqa: E731
-        loaded = [None] * n
+        loaded_x = [None] * n
+        loaded_g = [None] * n
         computed = [None] * n
         drained = [None] * n
 
@@ -236,9 +249,11 @@ class LatentMoELayer:
                 if i >= 2:
                     h2d.wait_event(computed[i - 2])  # slot s no longer read by step i-2
                 P["x"][s].copy_(x_host[i], non_blocking=True)
+                loaded_x[i] = ev()
+                loaded_x[i].record(h2d)
                 P["g"][s].copy_(g_host[i], non_blocking=True)
-                loaded[i] = ev()
-                loaded[i].record(h2d)
+                loaded_g[i] = ev()
+                loaded_g[i].record(h2d)
 
         keep = self.dx  # the eager steps write their input gradient into the slots
         load(0)
@@ -247,13 +262,17 @@ class LatentMoELayer:
                 s = i & 1
                 if i + 1 < n:
                     load(i + 1)
-                comp.wait_event(loaded[i])
+                comp.wait_event(loaded_x[i])
+                if graphs:
+                    self._pipe_graphs[s][0].replay()
+                else:
+                    self.forward(P["x"][s])
+                comp.wait_event(loaded_g[i])
                 if i >= 2:
                     comp.wait_event(drained[i - 2])  # dx slot s copied out by step i-2
                 if graphs:
-                    self._pipe_graphs[s].replay()
+                    self._pipe_graphs[s][1].replay()
                 else:
-                    self.forward(P["x"][s])
                     self.dx = P["dx"][s]
                     self.backward(P["g"][s])
                 computed[i] = ev()

@@ -34,6 +34,10 @@ def test_bench_workload_shape():
     # dy 536.87 + W2 939.52 + g,u,h in and dg,du,w*h out 1610.61 + d_row_w 1.05
     ("expert_dgrad2_swiglu_bwd", 274.88, 3088.06),
     ("routing_weight_grad_reduce", 0, 5.24),   # 4 fp32 partials in, 1 out, per row
+    ("permute_hist", 0, 1.28),                 # ids 1.05 + 64 chunks x 896 counts 0.23
+    ("permute_maps", 0, 5.48),                 # ids, weights 2.10 + prefixes 0.23 + maps out 3.15
+    # dW2_sh: 4 slices of 1024 x 1024 fp32 in + out 20.97; dW13_sh: 2 of 1024 x 2048 25.17
+    ("splitk_reduce", 0, 23.07),
 ])
 def test_kernel_work_matches_hand_computed_values(label, flops, nbytes):
     fl, by = bench.kernel_work(CFG, T)[label]
@@ -130,7 +134,9 @@ def test_kernel_work_bf16_weight_gradients():
     """With bf16 weight gradients only the gradient writes shrink, by half."""
     a, b = bench.kernel_work(CFG, T), bench.kernel_work(CFG, T, wgrad_bytes=2)
     grads = {"latent_proj_wgrad": d * l, "expert_wgrad2": E * f * l, "expert_wgrad1": E * l * 2 * f,
-             "shared_wgrad2": S * f * l, "shared_wgrad1": S * l * 2 * f, "router_wgrad": d * E}
+             "shared_wgrad2": S * f * l, "shared_wgrad1": S * l * 2 * f, "router_wgrad": d * E,
+             # the split-K reduction writes the shared gradients (mean of its two launches)
+             "splitk_reduce": (S * f * l + l * 2 * S * f) // 2}
     for label in a:
         assert a[label][0] == b[label][0], label
         assert a[label][1] - b[label][1] == 2 * grads.get(label, 0), label

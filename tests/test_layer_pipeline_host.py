@@ -53,11 +53,15 @@ class _Layer(LatentMoELayer):
         self.dx.copy_(self.x + dout)
         return self.dx
 
-    def capture_step(self, x, dout):
-        # a graph replays the step on the buffers it was captured with
+    def capture_halves(self, x, dout):
+        # the graphs replay the step on the buffers they were captured with:
+        # the forward keeps a copy of x, the backward writes dx = x + dout
         self.captures += 1
         dx = self.dx
-        return types.SimpleNamespace(replay=lambda: dx.copy_(x + dout))
+        seen = torch.zeros_like(x)
+        fwd = types.SimpleNamespace(replay=lambda: seen.copy_(x))
+        bwd = types.SimpleNamespace(replay=lambda: dx.copy_(seen + dout))
+        return fwd, bwd
 
 
 @pytest.mark.parametrize("graphs", [False, True])
