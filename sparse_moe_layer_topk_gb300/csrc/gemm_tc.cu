@@ -863,7 +863,9 @@ __device__ __forceinline__ void swiglu_bwd8(const float* a, uint4 G, uint4 U, ui
 // (32 rows x 32 columns, bf16, 64-byte rows with 64-byte swizzle) of one
 // 32-column chunk. Lane 0 loads them by TMA SLOTS - 1 chunks ahead of the chunk being
 // computed (across tile boundaries too). The chunk's dg, du and w*h overwrite g,
-// u and h in place and leave by TMA store from the same slot. (Loading the
+// u and h in place and leave by TMA store from the same slot. With the FP8 cache
+// the slot holds g and u as 32-byte rows of E4M3 (read by every lane before any
+// writes its outputs) and the row scales come with the tile. (Loading the
 // inputs lane by lane instead makes every load instruction touch 32 rows, so
 // the L1's request rate, not DRAM, sets the pace.)
 template <int BN, bool PAIR>
@@ -1100,14 +1102,14 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   const int q = warp & 3;  // tensor-memory lane quadrant this warp may read
   const int grp = (warp - 2) / 4;
   const uint32_t lane = lane_id();
-  uint8_t* const stg0 = staging + (warp - 2) * Cfg<BN, EW, CW16>::STG;
+  uint8_t* const stg0 = staging + (warp - 2) * Cfg<BN, EW, CW16, PAIR>::STG;
   // slot of one chunk (1 KB multiples keep every swizzle span aligned)
   int slot_bytes;
   if (p.epi == EPI_STORE) slot_bytes = p.c_bf16 ? 2048 : 4096;
   else if (p.epi == EPI_ROWSCALE) slot_bytes = 2048;
   else if (p.gu8) slot_bytes = 2048;  // EPI_SWIGLU, FP8 cache: h, g and u of 16 columns
   else slot_bytes = (CW16 ? 1024 : 2048) * (p.gu ? 3 : 1);  // EPI_SWIGLU
-  int nslots = Cfg<BN, EW, CW16>::STG / slot_bytes;
+  int nslots = Cfg<BN, EW, CW16, PAIR>::STG / slot_bytes;
   if (nslots > 4) nslots = 4;
   int slot = 0;
   uint8_t* stg = stg0;  // the current chunk's slot (set by stage_begin)
