@@ -204,6 +204,33 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// L2 policy for lines that should leave L2 first (outputs that nothing reads
+// again soon, written while other operands are being reused from L2).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// TMA tensor stores from shared memory with an L2 cache policy (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d_hint(const void* map, uint32_t src, int c0, int c1,
+                                                  uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], "
+      "%4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d_hint(const void* map, uint32_t src, int c0, int c1,
+                                                  int c2, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], "
+      "[%1], %5;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
+      : "memory");
+}
+
 // TMA tensor store from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

@@ -1177,7 +1177,10 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             if (p.c_bf16) stage_bf16(stg, lane, v); else stage_f32(stg, lane, v);
             stage_end();
             if (lane == 0) {
-              if (sm.c0_rank3) tma_store_3d(sm.c0, stg_s, ncol, row0, cb);
+              // weight gradients (grouped-K) are not read again in the step
+              if (p.sched == SCHED_GROUPED_K)
+                tma_store_3d_hint(sm.c0, stg_s, ncol, row0, cb, l2_policy_evict_first());
+              else if (sm.c0_rank3) tma_store_3d(sm.c0, stg_s, ncol, row0, cb);
               else tma_store_2d(sm.c0, stg_s, ncol, row0);
               bulk_commit();
             }
@@ -1261,12 +1264,14 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             stage_end();
             if (lane == 0) {
               tma_store_2d(sm.c0, stg_s, hcol, row0);
+              // the g|u cache is read by the backward only
+              const uint64_t pol = l2_policy_evict_first();
               if (p.gu8) {
-                tma_store_2d(sm.c1, stg_s + 1024, gcol, row0);
-                tma_store_2d(sm.c1, stg_s + 1536, gcol + p.f, row0);
+                tma_store_2d_hint(sm.c1, stg_s + 1024, gcol, row0, pol);
+                tma_store_2d_hint(sm.c1, stg_s + 1536, gcol + p.f, row0, pol);
               } else if (p.gu) {
-                tma_store_2d(sm.c1, stg_s + 1024, gcol, row0);
-                tma_store_2d(sm.c1, stg_s + 2048, gcol + p.f, row0);
+                tma_store_2d_hint(sm.c1, stg_s + 1024, gcol, row0, pol);
+                tma_store_2d_hint(sm.c1, stg_s + 2048, gcol + p.f, row0, pol);
               }
               bulk_commit();
             }
@@ -1305,9 +1310,10 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             stage_end();
             if (lane == 0) {
               tma_store_2d(sm.c0, stg_s, hcol, row0);
-              if (p.gu) {
-                tma_store_2d(sm.c1, stg_s + 2048, gcol, row0);
-                tma_store_2d(sm.c1, stg_s + 4096, gcol + p.f, row0);
+              if (p.gu) {  // the g|u cache is read by the backward only
+                const uint64_t pol = l2_policy_evict_first();
+                tma_store_2d_hint(sm.c1, stg_s + 2048, gcol, row0, pol);
+                tma_store_2d_hint(sm.c1, stg_s + 4096, gcol + p.f, row0, pol);
               }
               bulk_commit();
             }

@@ -379,7 +379,10 @@ __global__ void __launch_bounds__(kChunkThreads)
   }
 }
 
-// One warp per destination row; l/8 16-byte vectors per row.
+// One warp per destination row; l/8 16-byte vectors per row. The rows are
+// written with evict-first (streaming) stores: the permuted copy is several
+// times larger than L2 and is next read by another kernel, so its lines should
+// not displace the source, which every row is gathered from.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
                                                           const int* __restrict__ index,
                                                           long long R, int nvec,
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     }
     const uint4* s = src + static_cast<long long>(t) * nvec;
 #pragma unroll 4
-    for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
+    for (int v = lane; v < nvec; v += 32) __stcs(d + v, __ldg(s + v));
   }
 }
 
