@@ -405,7 +405,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 
 // One warp per token: lane j reads slot j of the token once; the rows are
 // summed four at a time (their loads issued together, the sums taken in slot
-// order), each lane owning up to 4 16-byte column vectors per pass.
+// order), each lane owning up to 4 16-byte column vectors per pass. The k rows
+// are read once, with evict-first (streaming) loads, so that they do not push
+// the small summed output, which the next GEMM reads, out of L2.
 __global__ void __launch_bounds__(256, 2) gather_sum_kernel(const uint4* __restrict__ src,
                                                             const int* __restrict__ slot, int k,
                                                             const uint4* __restrict__ add, int T,
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(256, 2) gather_sum_kernel(const uint4* __restr
         for (int i = 0; i < 4; ++i) {
           const int v = v0 + lane + 32 * i;
           x[u][i] = (j0 + u < k && r[u] >= 0 && v < nvec)
-                        ? __ldg(src + static_cast<long long>(r[u]) * nvec + v)
+                        ? __ldcs(src + static_cast<long long>(r[u]) * nvec + v)
                         : z4;
         }
 #pragma unroll
