@@ -222,7 +222,8 @@ int moe_grouped_swiglu(const uint16_t* z_perm, const uint16_t* W13, const uint16
  * ([SWAP]) instead of bf16: E4M3 (round to nearest even, saturating at +-448)
  * of g / s and u / s, with one power-of-two scale s per row and 64-feature block,
  * the smallest with max |block| <= 448 s (1 when that maximum is below 2^-100):
- *   gu8[r][c]               E4M3 bytes [R][2f] (columns as in gu_save)
+ *   gu8[r][32q + i]         E4M3 bytes [R][2f]: g[r][16q + i] (i < 16), u[r][16q + i - 16]
+ *                           (16 <= i < 32): 16-feature groups of g and u in turn
  *   gu_scale[r][b]          fp32 [R][2f/64]: blocks of g (b < f/64), then of u
  * h and y_perm are exactly those of moe_grouped_swiglu. f must be a multiple of
  * 128 (MOE_ERR_UNSUPPORTED otherwise); gu8 16-byte aligned. The cache takes 1 + 1/16

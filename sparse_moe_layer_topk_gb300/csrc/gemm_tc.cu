@@ -916,10 +916,11 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
     if (lane == 0) {
       const uint32_t d = smem_u32(slots + slot * SLOT);
       if (p.gu8) {
-        // FP8 cache: 32-byte rows of g and u at 0 and 1024, h at 4096
-        mbar_arrive_expect_tx(&lb[slot], 1024 + 1024 + 2048);
-        tma_load_2d(d, sm.ld_gu, &lb[slot], gcol, row0);
-        tma_load_2d(d + 1024, sm.ld_gu, &lb[slot], gcol + p.f, row0);
+        // FP8 cache: 64-byte rows of the chunk's interleaved g and u bytes (16 g, 16 u,
+        // 16 g, 16 u; byte column = gcol + the feature offset within the batch) at 0,
+        // h at 4096
+        mbar_arrive_expect_tx(&lb[slot], 2048 + 2048);
+        tma_load_2d(d, sm.ld_gu, &lb[slot], gcol + (n - sx * p.f), row0);
       } else {
         mbar_arrive_expect_tx(&lb[slot], SLOT);
         tma_load_2d(d, sm.ld_gu, &lb[slot], gcol, row0);
@@ -1002,14 +1003,17 @@ __device__ void epilogue_loop_sbwd(const Params& p, const StoreMaps& sm, uint8_t
         uint8_t* const sl = slots + slot * SLOT;
         uint8_t* const rowp = sl + lane * 64;
         bf16* dgdst = reinterpret_cast<bf16*>(p.C) + grow * p.ldc + gcol;
-        // FP8 cache: the lane's 32 g and 32 u bytes (rows of 32 bytes) are read
-        // before any lane writes its outputs over them; block scales per row
+        // FP8 cache: the lane's 32 g and 32 u bytes (one 64-byte row, 64-byte
+        // swizzle: 16-byte pieces g, u, g, u) are read before any lane writes its
+        // outputs over them; block scales per row
         uint32_t g8[8], u8[8];
         float sgl = 1.0f, sul = 1.0f;
         if (p.gu8) {
-          const uint4* const gp = reinterpret_cast<const uint4*>(sl + lane * 32);
-          const uint4* const up = reinterpret_cast<const uint4*>(sl + 1024 + lane * 32);
-          const uint4 g0 = gp[0], g1 = gp[1], u0 = up[0], u1 = up[1];
+          const uint8_t* const rp8 = sl + lane * 64;
+          const uint4 g0 = *reinterpret_cast<const uint4*>(rp8 + ((0 ^ sw) << 4));
+          const uint4 u0 = *reinterpret_cast<const uint4*>(rp8 + ((1 ^ sw) << 4));
+          const uint4 g1 = *reinterpret_cast<const uint4*>(rp8 + ((2 ^ sw) << 4));
+          const uint4 u1 = *reinterpret_cast<const uint4*>(rp8 + ((3 ^ sw) << 4));
           g8[0] = g0.x; g8[1] = g0.y; g8[2] = g0.z; g8[3] = g0.w;
           g8[4] = g1.x; g8[5] = g1.y; g8[6] = g1.z; g8[7] = g1.w;
           u8[0] = u0.x; u8[1] = u0.y; u8[2] = u0.z; u8[3] = u0.w;
@@ -1255,8 +1259,11 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             stage_begin();
             stage_bf16_16(stg, lane, hv);
             if (p.gu8) {
-              *reinterpret_cast<uint4*>(stg + 1024 + lane * 16) = f32x16_to_e4m3(g, inv_g);
-              *reinterpret_cast<uint4*>(stg + 1536 + lane * 16) = f32x16_to_e4m3(u, inv_u);
+              // one 32-byte row per lane: the 16 g bytes, then the 16 u bytes (32-byte swizzle)
+              const int sw = (static_cast<int>(lane) >> 2) & 1;
+              uint8_t* const rp = stg + 1024 + lane * 32;
+              *reinterpret_cast<uint4*>(rp + (sw << 4)) = f32x16_to_e4m3(g, inv_g);
+              *reinterpret_cast<uint4*>(rp + ((1 ^ sw) << 4)) = f32x16_to_e4m3(u, inv_u);
             } else if (p.gu) {
               stage_bf16_16(stg + 1024, lane, g);
               stage_bf16_16(stg + 2048, lane, u);
@@ -1267,8 +1274,8 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
               // the g|u cache is read by the backward only
               const uint64_t pol = l2_policy_evict_first();
               if (p.gu8) {
-                tma_store_2d_hint(sm.c1, stg_s + 1024, gcol, row0, pol);
-                tma_store_2d_hint(sm.c1, stg_s + 1536, gcol + p.f, row0, pol);
+                // byte column of feature j: 32 bytes per 16 features (g, then u)
+                tma_store_2d_hint(sm.c1, stg_s + 1024, gcol + j, row0, pol);
               } else if (p.gu) {
                 tma_store_2d_hint(sm.c1, stg_s + 1024, gcol, row0, pol);
                 tma_store_2d_hint(sm.c1, stg_s + 2048, gcol + p.f, row0, pol);
@@ -1279,8 +1286,8 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           } else if (row_ok) {
             store_bf16_row16(p.h + grow * p.ldh + hcol, hv);
             if (p.gu8) {
-              store16(p.gu8 + grow * p.ldgu + gcol, f32x16_to_e4m3(g, inv_g));
-              store16(p.gu8 + grow * p.ldgu + gcol + p.f, f32x16_to_e4m3(u, inv_u));
+              store16(p.gu8 + grow * p.ldgu + gcol + j, f32x16_to_e4m3(g, inv_g));
+              store16(p.gu8 + grow * p.ldgu + gcol + j + 16, f32x16_to_e4m3(u, inv_u));
             } else if (p.gu) {
               store_bf16_row16(p.gu + grow * p.ldgu + gcol, g);
               store_bf16_row16(p.gu + grow * p.ldgu + gcol + p.f, u);
@@ -1547,15 +1554,18 @@ bool make_store_map(CUtensorMap* map, void* ptr, bool f32, bool rank3, long long
 }
 
 // Tensor map of a byte matrix [d1][d0] (ld bytes between rows) for 32-row boxes
-// of box_cols bytes (16 or 32), no swizzle: the FP8 cache's blocks.
+// of box_cols bytes (32 or 64), swizzled over the box's row width: the FP8
+// cache's blocks (rows of interleaved 16-byte g and u groups).
 bool make_u8_map(CUtensorMap* map, void* ptr, long long d0, long long d1, long long ld,
                  int box_cols) {
+  if (box_cols != 32 && box_cols != 64) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 32};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -1713,7 +1723,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
     ok = make_store_map(&mapC0, L.h, false, false, L.ldh, rows_out, 1, L.ldh, 0, 16);
     if (ok && L.gu)
       ok = make_store_map(&mapC1, L.gu, false, false, L.ldgu, rows_out, 1, L.ldgu, 0, 16);
-    if (ok && L.gu8) ok = make_u8_map(&mapC1, L.gu8, L.ldgu, rows_out, L.ldgu, 16);
+    if (ok && L.gu8) ok = make_u8_map(&mapC1, L.gu8, L.ldgu, rows_out, L.ldgu, 32);
   } else if (L.epi == EPI_ROWSCALE) {
     ok = make_store_map(&mapC0, L.C, false, false, L.N, rows_out, 1, L.ldc, 0);
   } else {  // EPI_SWIGLU_BWD (32-column blocks)
@@ -1721,7 +1731,7 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
     if (ok && L.aux)
       ok = make_store_map(&mapC1, L.aux, false, false, L.ldaux, rows_out, 1, L.ldaux, 0);
     // the epilogue's inputs g|u (or their FP8 cache) and h, in the same 32 x 32 blocks
-    if (ok && L.gu8) ok = make_u8_map(&mapA2, L.gu8, L.ldgu, rows_out, L.ldgu, 32);
+    if (ok && L.gu8) ok = make_u8_map(&mapA2, L.gu8, L.ldgu, rows_out, L.ldgu, 64);
     else if (ok) ok = make_store_map(&mapA2, L.gu, false, false, L.ldgu, rows_out, 1, L.ldgu, 0);
     if (ok) ok = make_store_map(&mapB2, L.h, false, false, L.ldh, rows_out, 1, L.ldh, 0);
   }

@@ -44,8 +44,14 @@ def _e4m3_values():
 
 
 def _decode(gu8, scale):
-    """The cache's g|u values: E4M3 byte value times its block's scale."""
-    vals = _e4m3_values()[gu8.cpu().numpy()]
+    """The cache's g|u values ([R][2f]: g, then u): each row's bytes hold 16-feature
+    groups of g and u in turn (32 bytes per 16 features); E4M3 byte value times its
+    block's scale."""
+    b = gu8.cpu().numpy()
+    R, f2 = b.shape
+    grp = b.reshape(R, f2 // 32, 2, 16)
+    vals = _e4m3_values()[np.concatenate([grp[:, :, 0, :].reshape(R, -1),
+                                          grp[:, :, 1, :].reshape(R, -1)], axis=1)]
     return vals * np.repeat(scale.cpu().numpy().astype(np.float64), O.FP8_BLOCK, axis=1)
 
 
