@@ -174,3 +174,19 @@ def test_zero_tokens_enqueue_nothing(lib):
     assert lib.moe_unpermute_combine(P, P, None, 0, 4, 64, P, None) == M.MOE_OK
     assert lib.moe_unpermute_combine_bwd(P, P, 0, 4, 64, P, None) == M.MOE_OK
     assert lib.moe_permute_bwd(P, P, None, 0, 4, 64, P, None) == M.MOE_OK
+
+
+@pytest.mark.parametrize("T", [256, 1024, 2048, 4096, 16384, 65536])
+@pytest.mark.parametrize("l,f,S", [(1024, 512, 2), (256, 64, 1), (512, 256, 3)])
+def test_bench_split_k_rule_matches_the_library(lib, T, l, f, S):
+    """bench.py restates the library's K-slice rule for the shared experts' weight
+    gradients (to count the split-K reduction's bytes); the library's workspace size
+    for the shared-expert backward (dgu plus the larger of the two gradients' fp32
+    slices) must agree with it."""
+    import bench
+
+    cfg = type("Cfg", (), {"S": S, "f": f, "l": l})
+    up256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    slices = max((m * n * 4 * s if s > 1 else 0) for m, n, s in bench.splitk_shapes(cfg, T))
+    want = up256(T * S * f * 2 * 2) + up256(slices)
+    assert M.moe_workspace_size(M.MOE_OP_SHARED_SWIGLU_BWD, T=T, l=l, f=f, S=S) == want
