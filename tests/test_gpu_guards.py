@@ -138,6 +138,37 @@ def test_grouped_swiglu_writes_stay_in_bounds():
     g.check()
 
 
+def test_grouped_swiglu_fp8cache_writes_stay_in_bounds():
+    """The FP8 cache's bytes and scales (32-byte TMA rows, per-thread stores for the
+    ragged row blocks) and the backward that reads them."""
+    counts = np.array([0, 1, 63, 64, 65, 127, 129, 300, 0, 5])
+    E, l, f = len(counts), 128, 128
+    offsets = O.expert_offsets(counts)
+    sched = O.m_tiles_schedule(counts, 128)
+    R = int(offsets[-1])
+    z_perm = dev(_bf16(30, R, l))
+    W13, W2 = dev(_bf16(31, E, l, 2 * f, std=0.02)), dev(_bf16(32, E, f, l, std=0.02))
+    row_w = dev(torch.rand(R, generator=torch.Generator().manual_seed(4)) * 0.2 + 0.01)
+    off_d = dev(torch.from_numpy(offsets).int())
+    sch_d = dev(torch.from_numpy(sched).int())
+    g = Guarded()
+    gu8 = g.empty(R, 2 * f, dtype=torch.uint8)
+    sc = g.empty(R, 2 * f // O.FP8_BLOCK, dtype=torch.float32)
+    h = g.empty(R, f, dtype=torch.bfloat16)
+    y = g.empty(R, l, dtype=torch.bfloat16)
+    M.moe_grouped_swiglu_fp8cache(z_perm, W13, W2, off_d, sch_d, row_w, E, R, l, f, gu8, sc, h, y)
+    dy = dev(_bf16(33, R, l))
+    dz = g.empty(R, l, dtype=torch.bfloat16)
+    d_row_w = g.empty(R, dtype=torch.float32)
+    dW13 = g.empty(E, l, 2 * f, dtype=torch.float32)
+    dW2 = g.empty(E, f, l, dtype=torch.float32)
+    wsb = M.moe_workspace_size(M.MOE_OP_GROUPED_SWIGLU_BWD, T=R, k=1, f=f)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    M.moe_grouped_swiglu_bwd_fp8cache(dy, z_perm, W13, W2, gu8, sc, h, row_w, off_d, sch_d, E, R,
+                                      l, f, dz, d_row_w, dW13, dW2, M.MOE_DTYPE_F32, ws, wsb)
+    g.check()
+
+
 @pytest.mark.parametrize("T,l,f,S", [(77, 256, 128, 3), (1100, 512, 256, 2)])
 def test_shared_swiglu_writes_stay_in_bounds(T, l, f, S):
     z = dev(_bf16(30, T, l))
