@@ -114,6 +114,9 @@ def kernel_work(cfg, T, wgrad_bytes=4):
     g = wgrad_bytes
     return {
         "router_logits_gemm": (2 * T * d * E, T * d * b + d * E * b + T * E * 4),
+        # the router and the down-projection as one GEMM over [Wr | W_dn] (x read once)
+        "router_latent_gemm": (2 * T * d * (E + l),
+                               T * d * b + d * (E + l) * b + T * E * 4 + T * l * b),
         "topk_sigmoid": (0, T * E * 4 + T * k * 12),
         "latent_proj_gemm": (2 * T * d * l, T * d * b + d * l * b + T * l * b),
         "permute_gather": (0, T * l * b + R * l * b + R * 4),

@@ -119,6 +119,17 @@ int moe_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int
                    int k, int32_t* topk_idx, float* topk_w, float* topk_s, void* ws,
                    size_t ws_bytes, int32_t* err_flag, void* stream);
 
+/* moe_route_topk and the latent down-projection z[T][l] (bf16) = x @ W_dn[d][l]
+ * ([MODEL]: experts computed in the latent space; the projection reads the same x)
+ * in one call: when T > 128 and E is a multiple of 128 one GEMM over [Wr | W_dn]
+ * reads x once (logits and z are bit-identical to the two separate calls), else
+ * moe_router_logits + moe_latent_proj. Same workspace as moe_route_topk (the
+ * logits stay in it); l a multiple of 64; z 16-byte aligned. */
+int moe_route_topk_latent(const uint16_t* x, const uint16_t* Wr, const float* bias,
+                          const uint16_t* W_dn, int T, int d, int E, int k, int l,
+                          int32_t* topk_idx, float* topk_w, float* topk_s, uint16_t* z, void* ws,
+                          size_t ws_bytes, int32_t* err_flag, void* stream);
+
 /* Auxiliary load-balance loss of the routing stage ("大模型落地昇腾" page, section
  * "三、通信侧": an auxiliary loss that constrains the entropy of the routing
  * distribution), read as the negative entropy of the batch's mean routing

@@ -46,6 +46,8 @@ SIGNATURES = {
     "moe_router_logits": ([_P, _P, _I, _I, _I, _P, _P], _I),
     "moe_topk_from_logits": ([_P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_route_topk": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P, _P], _I),
+    "moe_route_topk_latent": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P, _P],
+                              _I),
     "moe_permute": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P], _I),
     "moe_permute_noalloc": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_latent_proj": ([_P, _P, _I, _I, _I, _P, _P], _I),
@@ -176,6 +178,12 @@ def moe_route_topk(x, Wr, bias, T, d, E, k, topk_idx, topk_w, topk_s, ws, ws_byt
                    err_flag=None, stream=None):
     _call("moe_route_topk", x, Wr, bias, T, d, E, k, topk_idx, topk_w, topk_s, ws, ws_bytes,
           err_flag, stream)
+
+
+def moe_route_topk_latent(x, Wr, bias, W_dn, T, d, E, k, l, topk_idx, topk_w, topk_s, z, ws,
+                          ws_bytes, err_flag=None, stream=None):
+    _call("moe_route_topk_latent", x, Wr, bias, W_dn, T, d, E, k, l, topk_idx, topk_w, topk_s, z,
+          ws, ws_bytes, err_flag, stream)
 
 
 def moe_permute(z, topk_idx, topk_w, T, l, E, k, z_perm, counts, offsets, slot_of, token_of,

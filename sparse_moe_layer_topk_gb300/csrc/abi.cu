@@ -210,6 +210,51 @@ int moe_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int
   return moe_topk_from_logits(L, bias, T, E, k, topk_idx, topk_w, topk_s, err_flag, stream);
 }
 
+int moe_route_topk_latent(const uint16_t* x, const uint16_t* Wr, const float* bias,
+                          const uint16_t* W_dn, int T, int d, int E, int k, int l,
+                          int32_t* topk_idx, float* topk_w, float* topk_s, uint16_t* z, void* ws,
+                          size_t ws_bytes, int32_t* err_flag, void* stream) {
+  MOE_REQUIRE(x && Wr && W_dn && z && topk_idx && topk_w && topk_s, MOE_ERR_ARG);
+  MOE_REQUIRE(T >= 0 && d > 0 && l > 0 && E > 0 && E <= 1024 && k >= 1 && k <= 32 && k <= E,
+              MOE_ERR_ARG);
+  MOE_REQUIRE(d % 64 == 0 && E % 64 == 0 && l % 64 == 0, MOE_ERR_ALIGN);
+  MOE_REQUIRE(al16(x) && al16(Wr) && al16(W_dn) && al16(z), MOE_ERR_ALIGN);
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(ws != nullptr, MOE_ERR_WORKSPACE);
+  MOE_REQUIRE(ws_bytes >= moe_workspace_size(MOE_OP_ROUTE_TOPK, T, d, 0, E, k, 0, 0),
+              MOE_ERR_WORKSPACE);
+  float* L = reinterpret_cast<float*>(ws);
+  cudaStream_t st = S(stream);
+  if (T > 128 && E % 128 == 0 && pick_bn(E + l) == 256) {  // CTA pairs: two row blocks or more
+    // one GEMM over [Wr | W_dn]: x is read once; columns < E are the fp32 logits,
+    // the rest the bf16 latent z
+    GemmLaunch G;
+    G.name = "router_latent_gemm";
+    G.BN = 256;
+    G.sched = SCHED_DENSE;
+    G.M = T;
+    G.N = E + l;
+    G.K = d;
+    G.A = view(x, T, d, d);
+    G.B = view(Wr, d, E, E);
+    G.b_mn = 1;
+    G.B2 = view(W_dn, d, l, l);
+    G.ncat = E;
+    G.epi = EPI_STORE;
+    G.C = L;
+    G.ldc = E;
+    G.c_bf16 = 0;
+    G.C2 = z;
+    G.ldc2 = l;
+    G.c2_bf16 = 1;
+    MOE_CHECK(gemm_launch(G, st));
+  } else {
+    MOE_CHECK(moe_router_logits(x, Wr, T, d, E, L, stream));
+    MOE_CHECK(moe_latent_proj(x, W_dn, T, d, l, z, stream));
+  }
+  return moe_topk_from_logits(L, bias, T, E, k, topk_idx, topk_w, topk_s, err_flag, stream);
+}
+
 int moe_router_aux_loss(const float* logits, const float* bias, int T, int E, float* p_mean,
                         float* loss, void* ws, size_t ws_bytes, void* stream) {
   MOE_REQUIRE(logits && p_mean && loss, MOE_ERR_ARG);

@@ -101,6 +101,14 @@ struct GemmLaunch {
   // accumulator. kcat must be a multiple of 64.
   int kcat = 0;
   MatView A2, B2;
+  // N concatenation (dense CTA pairs, MN-major B, plain stores): output columns
+  // n >= ncat come from B2 ([K][N - ncat]) and go to C2 ([M][ldc2], bf16 when
+  // c2_bf16) at column n - ncat; the others from B to C. ncat must be a multiple
+  // of 128, so that neither CTA's half of a tile's B columns straddles it.
+  int ncat = 0;
+  void* C2 = nullptr;
+  long long ldc2 = 0;
+  int c2_bf16 = 1;
   // Dense schedule with 256-wide tiles: run CTA pairs on 256-row tiles
   // (cta_group::2 MMAs; each CTA stages half of B). 0 forces single CTAs.
   int pair = 1;

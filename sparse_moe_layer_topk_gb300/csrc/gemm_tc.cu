@@ -94,6 +94,8 @@ struct Params {
   int mt, nt;         // m tiles (dense / grouped-K), n tiles
   int splitk, kslice; // dense: K split into `splitk` slices of `kslice` (multiple of 64)
   int kcat;           // dense: K index where A/B switch to the second operand pair (0: none)
+  int ncat;           // dense pairs: output column where B / C switch to B2 / C2 (0: none)
+  int c2_bf16;        // C2 holds bf16 (else fp32)
   int total_static;   // tile count when it does not depend on device data
   int epi;
   void* C;
@@ -345,6 +347,8 @@ __device__ void producer_loop(const Params& p, const CUtensorMap* mapA, const CU
             const int c0 =
                 (p.swiglu_b ? (half_n == 0 ? ti.nb0 : p.f + ti.nb0) : ti.nb0 + half_n) >> 6;
             if (p.b_rank3) tma_load_4d_pair(sB, mapB, fb, 0, kb_coord, c0, batch);
+            else if (p.ncat > 0 && c0 * 64 >= p.ncat)  // this half's columns are B2's
+              tma_load_3d_pair(sB, mapB2, fb, 0, kb_coord, c0 - p.ncat / 64);
             else tma_load_3d_pair(sB, mapB, fb, 0, kb_coord, c0);
           }
         }
@@ -1109,7 +1113,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
   uint8_t* const stg0 = staging + (warp - 2) * Cfg<BN, EW, CW16, PAIR>::STG;
   // slot of one chunk (1 KB multiples keep every swizzle span aligned)
   int slot_bytes;
-  if (p.epi == EPI_STORE) slot_bytes = p.c_bf16 ? 2048 : 4096;
+  if (p.epi == EPI_STORE) slot_bytes = (p.c_bf16 && (p.ncat == 0 || p.c2_bf16)) ? 2048 : 4096;
   else if (p.epi == EPI_ROWSCALE) slot_bytes = 2048;
   else if (p.gu8) slot_bytes = 2048;  // EPI_SWIGLU, FP8 cache: h, g and u of 16 columns
   else slot_bytes = (CW16 ? 1024 : 2048) * (p.gu ? 3 : 1);  // EPI_SWIGLU
@@ -1170,7 +1174,10 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
           int ncol = n, cb = 0;
-          if (p.sched == SCHED_GROUPED_K || p.splitk > 1) {
+          const bool second = p.ncat > 0 && n >= p.ncat;  // a column of C2
+          if (second) {
+            ncol = n - p.ncat;
+          } else if (p.sched == SCHED_GROUPED_K || p.splitk > 1) {
             cb = ti.g;  // expert (grouped-K) or K slice (split-K partials)
           } else if (p.c_batch_n > 0) {
             cb = n / p.c_batch_n;
@@ -1178,11 +1185,12 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           }
           if (use_tma && !p.accumulate) {
             stage_begin();
-            if (p.c_bf16) stage_bf16(stg, lane, v); else stage_f32(stg, lane, v);
+            if (second ? p.c2_bf16 : p.c_bf16) stage_bf16(stg, lane, v); else stage_f32(stg, lane, v);
             stage_end();
             if (lane == 0) {
               // weight gradients (grouped-K) are not read again in the step
-              if (p.sched == SCHED_GROUPED_K)
+              if (second) tma_store_2d(sm.c1, stg_s, ncol, row0);
+              else if (p.sched == SCHED_GROUPED_K)
                 tma_store_3d_hint(sm.c0, stg_s, ncol, row0, cb, l2_policy_evict_first());
               else if (sm.c0_rank3) tma_store_3d(sm.c0, stg_s, ncol, row0, cb);
               else tma_store_2d(sm.c0, stg_s, ncol, row0);
@@ -1678,6 +1686,18 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
       return MOE_ERR_ARG;
     p.kcat = L.kcat;
   }
+  p.ncat = 0;
+  p.c2_bf16 = L.c2_bf16;
+  if (L.ncat > 0) {
+    // N-concatenated second operand: dense CTA pairs, MN-major B and B2, plain stores
+    if (!PAIR || L.sched != SCHED_DENSE || L.epi != EPI_STORE || L.accumulate ||
+        p.splitk > 1 || L.kcat > 0 || !L.b_mn || L.b_batch_mode != BATCH_NONE ||
+        L.swiglu_b || L.gather_a || L.gather_b || L.c_batch_n > 0 || L.ncat % 128 != 0 ||
+        L.ncat >= L.N || !L.C2 || L.ldc2 < L.N - L.ncat)
+      return MOE_ERR_UNSUPPORTED;
+    if (!make_map_chunked(&mapB2, L.B2, BN / 128, false)) return MOE_ERR_ARG;
+    p.ncat = L.ncat;
+  }
   // (a gathered operand is copied by the gather warps, not by TMA: its map is
   // encoded only so that every map the kernel receives is a valid one.) Other
   // MN-major operands are read through a chunked map when their columns allow
@@ -1715,6 +1735,9 @@ int launch_bn(const GemmLaunch& L, cudaStream_t stream) {
         p.c0_rank3 = 1;
         ok = make_store_map(&mapC0, L.C, f32, true, L.c_batch_n, L.M, L.N / L.c_batch_n, L.ldc,
                             L.c_batch_stride);
+      } else if (L.ncat > 0) {
+        ok = make_store_map(&mapC0, L.C, f32, false, L.ncat, rows_out, 1, L.ldc, 0) &&
+             make_store_map(&mapC1, L.C2, !L.c2_bf16, false, L.N - L.ncat, rows_out, 1, L.ldc2, 0);
       } else {
         ok = make_store_map(&mapC0, L.C, f32, false, L.N, rows_out, 1, L.ldc, 0);
       }

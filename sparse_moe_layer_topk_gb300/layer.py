@@ -110,13 +110,14 @@ class LatentMoELayer:
         w, T, k, d, l, f, E, S, R = (self.w, self.T, self.k, self.d, self.l, self.f, self.E,
                                      self.S, self.R)
         self.x = x
-        M.moe_route_topk(x, w["Wr"], w.get("bias"), T, d, E, k, self.topk_idx, self.topk_w,
-                         self.topk_s, self.ws["route"], self.ws_sizes["route"], self.err, stream)
+        # router logits, top-k and the latent z = x W_dn (one GEMM over [Wr | W_dn])
+        M.moe_route_topk_latent(x, w["Wr"], w.get("bias"), w["W_dn"], T, d, E, k, l,
+                                self.topk_idx, self.topk_w, self.topk_s, self.z, self.ws["route"],
+                                self.ws_sizes["route"], self.err, stream)
         if self.aux_scale > 0:
             # the router logits stay in the route workspace until the backward
             M.moe_router_aux_loss(self.ws["route"], w.get("bias"), T, E, self.p_mean, self.aux_loss,
                                   self.ws["aux"], self.ws_sizes["aux"], stream)
-        M.moe_latent_proj(x, w["W_dn"], T, d, l, self.z, stream)
         fused = self.fused_gather
         M.moe_permute(None if fused else self.z, self.topk_idx, self.topk_w, T, l, E, k,
                       self.z_perm, self.counts, self.offsets, self.slot_of, self.token_of,

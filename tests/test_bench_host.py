@@ -23,6 +23,8 @@ def test_bench_workload_shape():
     ("router_logits_gemm", 120.26, None),      # 2 * 16384 * 4096 * 896
     ("topk_sigmoid", 0, 61.87),                # 16384*896*4 + 16384*16*12
     ("latent_proj_gemm", 137.44, None),        # 2 * 16384 * 4096 * 1024
+    # x 134.22 + [Wr | W_dn] 15.73 + fp32 logits 58.72 + bf16 z 33.55
+    ("router_latent_gemm", 257.70, 242.22),    # 2 * 16384 * 4096 * (896 + 1024)
     ("permute_gather", 0, 571.47),             # 33.55 + 536.87 + 1.05
     ("combine", 0, 605.03),                    # 536.87 + 2*33.55 + 1.05
     ("expert_gemm1_swiglu", 549.76, None),     # 2 * 262144 * 1024 * 1024

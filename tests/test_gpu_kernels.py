@@ -64,6 +64,40 @@ def test_router_logits():
     assert err < 1e-4, err
 
 
+
+@pytest.mark.parametrize("T,d,E,l,k", [(300, 256, 256, 256, 4), (1100, 512, 384, 512, 8),
+                                       (2048, 4096, 896, 1024, 16), (100, 256, 256, 256, 4),
+                                       (300, 256, 64, 256, 4), (1, 128, 128, 64, 2)])
+def test_route_topk_latent_equals_the_separate_calls(T, d, E, l, k):
+    """The router and the latent down-projection as one GEMM over [Wr | W_dn]
+    (T > 128, E a multiple of 128: columns of the 256-wide tile that straddles E
+    come from both weights) give the separate calls' logits, z and selection bit
+    for bit; the other shapes take the separate calls inside the entry point.
+    The logits against the oracle as in test_router_logits."""
+    x = dev(_bf16(40, T, d))
+    Wr = dev(_bf16(41, d, E, std=0.02))
+    W_dn = dev(_bf16(42, d, l, std=0.02))
+    wsb = M.moe_workspace_size(M.MOE_OP_ROUTE_TOPK, T=T, d=d, E=E, k=k)
+    ws0 = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    ws1 = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    out = []
+    for ws, fused in ((ws0, False), (ws1, True)):
+        idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+        w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+        sg = torch.empty(T, k, dtype=torch.float32, device="cuda")
+        z = torch.empty(T, l, dtype=torch.bfloat16, device="cuda")
+        if fused:
+            M.moe_route_topk_latent(x, Wr, None, W_dn, T, d, E, k, l, idx, w, sg, z, ws, wsb)
+        else:
+            M.moe_route_topk(x, Wr, None, T, d, E, k, idx, w, sg, ws, wsb)
+            M.moe_latent_proj(x, W_dn, T, d, l, z)
+        out.append((ws[: T * E * 4].view(torch.float32).view(T, E).clone(), idx, w, sg, z))
+    torch.cuda.synchronize()
+    for name, a, b in zip(("logits", "topk_idx", "topk_w", "topk_s", "z"), out[0], out[1]):
+        assert torch.equal(a, b), name
+    err = np.abs(f64(out[1][0]) - O.router_logits(x.cpu(), Wr.cpu())).max()
+    assert err < 1e-4, err
+
 # ---------------------------------------------------------------- top-k
 
 @pytest.mark.parametrize("T,E,k,ties,bias", [
