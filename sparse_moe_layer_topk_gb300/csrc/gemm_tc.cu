@@ -1161,7 +1161,28 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
     const bool use_tma = qr == 32 && (blk_rows >= 32 || p.sched != SCHED_GROUPED_M);
 
     if (blk_rows > 0) {
-      if (p.epi == EPI_STORE) {
+      if (p.epi == EPI_STORE && p.ncat > 0) {
+        // N-concatenated outputs (dense CTA pairs; TMA stores, which clip the rows
+        // past M): columns below ncat go to C, the others to C2 at n - ncat. A loop
+        // of its own keeps the plain stores' loop below as it is.
+#pragma unroll 1
+        for (int c = grp; c < BN / 32; c += NG) {
+          const int n = ti.nb0 + c * 32;
+          if (n >= p.N) break;
+          float v[32];
+          ld_chunk(trow + c * 32, v);
+          const bool second = n >= p.ncat;
+          stage_begin();
+          if (second ? p.c2_bf16 : p.c_bf16) stage_bf16(stg, lane, v); else stage_f32(stg, lane, v);
+          stage_end();
+          if (lane == 0) {
+            if (second) tma_store_2d(sm.c1, stg_s, n - p.ncat, row0);
+            else tma_store_2d(sm.c0, stg_s, n, row0);
+            bulk_commit();
+          }
+          pending = true;
+        }
+      } else if (p.epi == EPI_STORE) {
 #pragma unroll 1
         for (int c = grp; c < BN / 32; c += NG) {
           const int n = ti.nb0 + c * 32;
@@ -1174,10 +1195,7 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
           int ncol = n, cb = 0;
-          const bool second = p.ncat > 0 && n >= p.ncat;  // a column of C2
-          if (second) {
-            ncol = n - p.ncat;
-          } else if (p.sched == SCHED_GROUPED_K || p.splitk > 1) {
+          if (p.sched == SCHED_GROUPED_K || p.splitk > 1) {
             cb = ti.g;  // expert (grouped-K) or K slice (split-K partials)
           } else if (p.c_batch_n > 0) {
             cb = n / p.c_batch_n;
@@ -1185,12 +1203,11 @@ __device__ void epilogue_loop(const Params& p, const StoreMaps& sm, uint8_t* sta
           }
           if (use_tma && !p.accumulate) {
             stage_begin();
-            if (second ? p.c2_bf16 : p.c_bf16) stage_bf16(stg, lane, v); else stage_f32(stg, lane, v);
+            if (p.c_bf16) stage_bf16(stg, lane, v); else stage_f32(stg, lane, v);
             stage_end();
             if (lane == 0) {
               // weight gradients (grouped-K) are not read again in the step
-              if (second) tma_store_2d(sm.c1, stg_s, ncol, row0);
-              else if (p.sched == SCHED_GROUPED_K)
+              if (p.sched == SCHED_GROUPED_K)
                 tma_store_3d_hint(sm.c0, stg_s, ncol, row0, cb, l2_policy_evict_first());
               else if (sm.c0_rank3) tma_store_3d(sm.c0, stg_s, ncol, row0, cb);
               else tma_store_2d(sm.c0, stg_s, ncol, row0);
